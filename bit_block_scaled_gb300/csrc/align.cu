@@ -1,0 +1,151 @@
+// Step a2: align/permute routed rows into per-expert blocks, then gather the
+// token rows (vLLM issue "moe_wna16_marlin_gemm applies wrong per-row topk
+// weights", "Minimal repro": moe_align_block_size and the sorted_ids /
+// expert_ids it produces).
+//
+// align_kernel is one CTA of 1024 threads: a shared-memory expert histogram,
+// a warp prefix sum of the block-padded counts, then a stable placement of
+// the flat rows in chunks of 1024 -- the rank of a row among earlier rows of
+// the same expert comes from __match_any_sync inside a warp and a per-expert
+// prefix over the 32 warps -- so the layout does not depend on thread timing.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe4 {
+
+namespace {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kMaxE = 256;
+
+__global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__restrict__ ids, int R, int E,
+                                                              int bm, int P_max, int32_t *__restrict__ sorted,
+                                                              int32_t *__restrict__ offsets,
+                                                              int32_t *__restrict__ block_ids,
+                                                              int32_t *__restrict__ row_pos,
+                                                              unsigned int *status) {
+  __shared__ int cnt[kMaxE];
+  __shared__ int off[kMaxE + 1];
+  __shared__ int base[kMaxE];
+  __shared__ int wcnt[32 * kMaxE];  // [warp][expert]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  for (int e = tid; e < E; e += kAlignThreads) cnt[e] = 0;
+  __syncthreads();
+  for (int r = tid; r < R; r += kAlignThreads) {
+    const int e = ids[r];
+    if (e < 0 || e >= E) {
+      raise_status(status, MOE_ERR_BAD_INDEX);
+      row_pos[r] = -1;
+    } else {
+      atomicAdd(&cnt[e], 1);  // integer counts: order-independent
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int running = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int pc = (e < E) ? (cnt[e] + bm - 1) / bm * bm : 0;
+      int incl = pc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) off[e] = running + incl - pc;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) off[E] = running;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += kAlignThreads) offsets[e] = off[e];
+  for (int e = tid; e < E; e += kAlignThreads) base[e] = off[e];
+  for (int q = tid; q < P_max; q += kAlignThreads) sorted[q] = R;
+  const int nb = P_max / bm;
+  for (int b = tid; b < nb; b += kAlignThreads) {
+    const int s = b * bm;
+    int be = -1;
+    if (s < off[E]) {
+      int lo = 0, hi = E - 1;  // largest e with off[e] <= s
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= s) lo = mid; else hi = mid - 1;
+      }
+      be = lo;
+    }
+    block_ids[b] = be;
+  }
+  __syncthreads();
+
+  for (int c0 = 0; c0 < R; c0 += kAlignThreads) {
+    const int r = c0 + tid;
+    int e = -1;
+    if (r < R) {
+      e = ids[r];
+      if (e < 0 || e >= E) e = -1;
+    }
+    for (int i = tid; i < 32 * E; i += kAlignThreads) wcnt[i] = 0;
+    __syncthreads();
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int e2 = tid; e2 < E; e2 += kAlignThreads) {
+      int run = base[e2];
+      for (int w = 0; w < 32; ++w) {
+        const int c = wcnt[w * E + e2];
+        wcnt[w * E + e2] = run;
+        run += c;
+      }
+      base[e2] = run;
+    }
+    __syncthreads();
+    if (e >= 0) {
+      const int pos = wcnt[warp * E + e] + rank;
+      sorted[pos] = r;
+      row_pos[r] = pos;
+    }
+    __syncthreads();
+  }
+}
+
+// x_perm[p] = x[sorted[p] / k], zero for padding slots; slots past the last
+// used one (offsets[E]) are never read by the GEMMs and are skipped.
+__global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x, int R, int k, int H8,
+                                                     const int32_t *__restrict__ sorted,
+                                                     const int32_t *__restrict__ used_end,
+                                                     uint4 *__restrict__ x_perm) {
+  const int p = blockIdx.x;
+  if (p >= *used_end) return;
+  const int s = sorted[p];
+  uint4 *dst = x_perm + (size_t)p * H8;
+  if (s >= 0 && s < R) {
+    const uint4 *src = x + (size_t)(s / k) * H8;
+    for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = src[v];
+  } else {
+    for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+}  // namespace
+
+moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, int P_max,
+                          int32_t *sorted_ids, int32_t *offsets, int32_t *block_ids, int32_t *row_pos,
+                          unsigned int *status, cudaStream_t stream, int *launches) {
+  align_kernel<<<1, kAlignThreads, 0, stream>>>(ids, T * k, E, block_m, P_max, sorted_ids, offsets, block_ids,
+                                                row_pos, status);
+  if (launches) ++*launches;
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
+                           const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches) {
+  if (P_max == 0) return MOE_OK;
+  gather_kernel<<<P_max, 128, 0, stream>>>(reinterpret_cast<const uint4 *>(x), T * k, k, H / 8, sorted_ids,
+                                           offsets_end, reinterpret_cast<uint4 *>(x_perm));
+  if (launches) ++*launches;
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe4

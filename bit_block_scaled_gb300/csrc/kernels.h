@@ -1,0 +1,51 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe4.h"
+
+namespace moe4 {
+
+struct GemmArgs {
+  CUtensorMap tm_w;  // packed 4-bit weights [E][N][K/2]
+  CUtensorMap tm_x;  // bf16 activations [P_max][K]
+  const void *scales;
+  const uint8_t *zeros;
+  const float *gscale;
+  const uint16_t *bias;
+  const int32_t *expert_offsets;
+  const int32_t *sorted_ids;
+  const float *topk_w;
+  uint16_t *out;
+  unsigned int *status;
+  int E, N, K, P_max, num_rows, ldo, layout, I, mul;
+  float alpha, limit;
+  int tile_n, stages, sc_row_bytes, z_row_bytes;
+};
+
+int choose_tile_n(int num_rows, int E);
+
+// epi: 0 = GEMM1 + swigluoai, 1 = GEMM1 + ReLU^2, 2 = GEMM2 + routing weight
+moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t *x, int P_max,
+                                 const int32_t *sorted_ids, const int32_t *expert_offsets, int num_rows,
+                                 const float *topk_w, int mul, int layout, moe_act_t act, uint16_t *out,
+                                 int ldo, unsigned int *status, cudaStream_t stream, int *launches);
+
+moe_status_t launch_route(const float *logits, const float *sel_bias, int T, int E, int k, int route,
+                          int32_t *ids, float *weights, unsigned int *status, cudaStream_t stream,
+                          int *launches);
+
+moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, int P_max,
+                          int32_t *sorted_ids, int32_t *offsets, int32_t *block_ids, int32_t *row_pos,
+                          unsigned int *status, cudaStream_t stream, int *launches);
+
+moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
+                           const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches);
+
+moe_status_t launch_unpermute(const uint16_t *y, const int32_t *row_pos, int T, int k, int H, int P_max,
+                              uint16_t *out, unsigned int *status, cudaStream_t stream, int *launches);
+
+}  // namespace moe4

@@ -1,0 +1,115 @@
+// Step a1: top-k routing, one warp per token.
+//
+// TOPK_SOFTMAX (gpt-oss; vLLM issue "moe_wna16_marlin_gemm applies wrong
+// per-row topk weights", "Minimal repro"): the k largest logits, descending,
+// equal values -> lower expert id, then a softmax over the k selected.
+// SIGMOID_BIAS (Nemotron-3-Nano; vLLM issue "... non-gated ReLU2 MoE
+// (Nemotron-3-Nano)", Analysis item 3, n_group = 1): s = sigmoid(logit) in
+// fp32, select by s + bias, weights = selected s renormalised to sum 1.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe4 {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kMaxPerLane = 8;  // E <= 256
+constexpr int kMaxK = 8;
+
+__device__ __forceinline__ float sigmoid_f32(float l) { return 1.0f / (1.0f + expf(-l)); }
+
+template <int ROUTE>
+__global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restrict__ logits,
+                                                            const float *__restrict__ sel_bias, int T, int E,
+                                                            int k, int32_t *__restrict__ ids,
+                                                            float *__restrict__ weights) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float *row = logits + (size_t)t * E;
+  float sc[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    float v = -INFINITY;
+    if (e < E) {
+      const float l = row[e];
+      v = (ROUTE == MOE_ROUTE_SIGMOID_BIAS) ? sigmoid_f32(l) + sel_bias[e] : l;
+      if (v != v) v = -INFINITY;  // NaN never outranks a number
+    }
+    sc[i] = v;
+  }
+  unsigned taken = 0;
+  int sel_id[kMaxK];
+  float sel_v[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j >= k) break;
+    float best = -INFINITY;
+    int bid = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (sc[i] > best || (sc[i] == best && e < bid))) {
+        best = sc[i];
+        bid = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+      if (ov > best || (ov == best && oid < bid)) {
+        best = ov;
+        bid = oid;
+      }
+    }
+    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+    sel_id[j] = bid;
+    sel_v[j] = (ROUTE == MOE_ROUTE_SIGMOID_BIAS) ? sigmoid_f32(row[bid]) : best;
+  }
+  if (lane != 0) return;
+  float w[kMaxK];
+  float sum = 0.f;
+  if (ROUTE == MOE_ROUTE_SIGMOID_BIAS) {
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k) {
+        w[j] = sel_v[j];
+        sum += w[j];
+      }
+  } else {
+    const float m = sel_v[0];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k) {
+        w[j] = expf(sel_v[j] - m);
+        sum += w[j];
+      }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < k) {
+      ids[(size_t)t * k + j] = sel_id[j];
+      weights[(size_t)t * k + j] = w[j] / sum;
+    }
+}
+
+}  // namespace
+
+moe_status_t launch_route(const float *logits, const float *sel_bias, int T, int E, int k, int route,
+                          int32_t *ids, float *weights, unsigned int *status, cudaStream_t stream,
+                          int *launches) {
+  (void)status;
+  if (T == 0) return MOE_OK;
+  const dim3 grid((T + kWarps - 1) / kWarps), block(kWarps * 32);
+  if (route == MOE_ROUTE_SIGMOID_BIAS)
+    route_kernel<MOE_ROUTE_SIGMOID_BIAS><<<grid, block, 0, stream>>>(logits, sel_bias, T, E, k, ids, weights);
+  else
+    route_kernel<MOE_ROUTE_TOPK_SOFTMAX><<<grid, block, 0, stream>>>(logits, sel_bias, T, E, k, ids, weights);
+  if (launches) ++*launches;
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe4

@@ -1,0 +1,258 @@
+"""GPU parity: every step of the CUDA path through the C ABI against the oracle.
+
+Integer work (routing ids, sorted ids, offsets, block ids, row positions, the
+x_perm gather) must be bit-exact; floating-point outputs must satisfy
+|gpu - oracle| <= 1e-2 + 1e-2 |oracle| with no NaN/Inf.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import (OR, assert_close, built, get_config, gpu_forward, gpu_steps, make,
+                         near_tie_ok, oracle_full, ws_status)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    return built()
+
+
+def _check_steps(g, o, cfg, exact_routing=True):
+    if exact_routing:
+        assert np.array_equal(g["topk_ids"], o["topk_ids"])
+    np.testing.assert_allclose(g["topk_weights"], o["topk_weights"], rtol=2e-6, atol=1e-7)
+    assert np.array_equal(g["sorted_token_ids"], o["sorted_token_ids"])
+    assert np.array_equal(g["expert_offsets"], o["expert_offsets"])
+    assert np.array_equal(g["block_expert_ids"], o["block_expert_ids"])
+    assert np.array_equal(g["row_pos"], o["row_pos"])
+    used = int(o["expert_offsets"][-1])
+    assert np.array_equal(g["x_perm"][:used], o["x_perm"][:used])
+    valid = o["sorted_token_ids"] < cfg.T * cfg.k
+    assert_close(g["a"][valid], o["a"][valid], "a (GEMM1 + act)")
+    assert_close(g["y"][valid], o["y"][valid], "y (GEMM2 + weight)")
+    assert_close(g["out"], o["out"], "out")
+    assert g["status"] == 0
+
+
+def test_c0_tiny_layer_steps():
+    cfg = get_config("c0")
+    L, N = make(cfg)
+    g = gpu_steps(L, cfg)
+    o = oracle_full(N, cfg)
+    _check_steps(g, o, cfg)
+
+
+def test_c0_forward_matches_steps_bit_exact():
+    cfg = get_config("c0")
+    L, N = make(cfg)
+    g = gpu_steps(L, cfg)
+    out, ws = gpu_forward(L, cfg)
+    assert np.array_equal(out.float().cpu().numpy(), g["out"])
+
+
+def test_gemm2_from_oracle_intermediates():
+    """The minimum slice: GEMM2 fed with the oracle's own a and metadata."""
+    import bit_block_scaled_gb300 as moe
+    cfg = get_config("c0")
+    L, N = make(cfg)
+    o = oracle_full(N, cfg)
+    dev = "cuda"
+    a = torch.from_numpy(o["a"]).to(torch.bfloat16).to(dev)
+    sorted_ids = torch.from_numpy(o["sorted_token_ids"]).to(dev)
+    offs = torch.from_numpy(o["expert_offsets"]).to(dev)
+    tw = torch.from_numpy(o["topk_weights"].reshape(-1)).to(dev)
+    y = torch.zeros(a.shape[0], cfg.H, dtype=torch.bfloat16, device=dev)
+    ws = ws_status()
+    moe.moe_grouped_gemm2_weighted(a, sorted_ids, offs, L["w2"], tw, 1, cfg.T * cfg.k, y, ws)
+    valid = o["sorted_token_ids"] < cfg.T * cfg.k
+    assert_close(y.float().cpu().numpy()[valid], o["y"][valid], "y")
+    assert moe.moe_read_status(ws) == 0
+
+
+FORMATS = [
+    # fmt, act, H, I, E, T, k, layout
+    ("nvfp4", "swigluoai", 320, 192, 5, 37, 2, 0),
+    ("nvfp4", "swigluoai", 320, 192, 5, 37, 2, 1),
+    ("nvfp4", "relu2", 192, 320, 6, 29, 3, 0),
+    ("mxfp4", "swigluoai", 384, 256, 4, 41, 2, 0),
+    ("mxfp4", "relu2", 256, 192, 7, 23, 2, 0),
+    ("int4", "swigluoai", 320, 256, 5, 33, 2, 0),
+    ("int4", "relu2", 448, 192, 4, 19, 3, 0),
+]
+
+
+@pytest.mark.parametrize("fmt,act,H,I,E,T,k,layout", FORMATS)
+def test_formats_and_activations(fmt, act, H, I, E, T, k, layout):
+    route = "sigmoid_bias" if act == "relu2" else "topk_softmax"
+    cfg = get_config("c0", name=f"fmt_{fmt}_{act}_{H}_{I}", fmt=fmt, act=act, H=H, I=I, E=E, T=T,
+                     k=k, route=route, sel_bias_std=0.1 if route == "sigmoid_bias" else 0.0,
+                     bias=(act == "swigluoai"))
+    L, N = make(cfg, seed=3)
+    if layout == 1:
+        # the same weights stored [gate; up]
+        idx = torch.cat([torch.arange(0, 2 * I, 2), torch.arange(1, 2 * I, 2)]).cuda()
+        w = dict(L["w13"])
+        for key in ("q", "scales", "zeros", "bias"):
+            if w.get(key) is not None:
+                w[key] = w[key][:, idx].contiguous()
+        L = dict(L)
+        L["w13"] = w
+    g = gpu_steps(L, cfg, layout=layout)
+    ids = g["topk_ids"].astype(np.int32)
+    o = oracle_full(N, cfg, ids=ids, tw=g["topk_weights"])
+    oref = oracle_full(N, cfg)
+    if cfg.route == "sigmoid_bias":
+        scores = OR.selection_scores(N["logits"], N["sel_bias"])
+        assert near_tie_ok(scores, ids, oref["topk_ids"]) == []
+    else:
+        assert np.array_equal(ids, oref["topk_ids"])
+    np.testing.assert_allclose(g["topk_weights"], oref["topk_weights"], rtol=2e-6, atol=1e-7) \
+        if np.array_equal(ids, oref["topk_ids"]) else None
+    _check_steps(g, o, cfg, exact_routing=False)
+
+
+def test_c1_decode_layer_full():
+    cfg = get_config("c1")
+    L, N = make(cfg)
+    g = gpu_steps(L, cfg)
+    o = oracle_full(N, cfg)
+    _check_steps(g, o, cfg)
+
+
+@pytest.mark.parametrize("block_m", [16, 32, 64, 128, 256])
+def test_block_m_sweep_same_output(block_m):
+    cfg = get_config("c0", name="bm_sweep", T=40, E=6, k=2, H=192, I=128)
+    L, N = make(cfg, seed=5)
+    out, ws = gpu_forward(L, cfg, block_m=block_m)
+    ref, _ = gpu_forward(L, cfg, block_m=16)
+    assert np.array_equal(out.float().cpu().numpy(), ref.float().cpu().numpy())
+
+
+def test_determinism_bit_identical():
+    cfg = get_config("c0", name="det", T=300, E=8, k=2, H=256, I=192)
+    L, N = make(cfg, seed=6)
+    a, _ = gpu_forward(L, cfg)
+    b, _ = gpu_forward(L, cfg)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_one_expert_takes_all_rows_spans_tiles():
+    """All 600 routed rows on expert 2: the token dimension splits into several
+    tiles of at most 256 rows with a ragged last tile."""
+    cfg = get_config("c0", name="hot", T=300, E=4, k=2, H=192, I=128)
+    L, N = make(cfg, seed=7)
+    L["logits"][:, 2] += 100.0
+    N["logits"][:, 2] += 100.0
+    g = gpu_steps(L, cfg)
+    o = oracle_full(N, cfg)
+    _check_steps(g, o, cfg)
+
+
+def test_top1_and_top8():
+    for k, E in ((1, 4), (8, 16)):
+        cfg = get_config("c0", name=f"k{k}", T=21, E=E, k=k, H=128, I=128)
+        L, N = make(cfg, seed=8)
+        g = gpu_steps(L, cfg)
+        o = oracle_full(N, cfg)
+        _check_steps(g, o, cfg)
+        if k == 1:
+            assert np.all(g["topk_weights"] == 1.0)
+
+
+def test_external_multiply_and_applied_ratio():
+    """mul_topk_weights=False + external multiply agrees with the fused
+    multiply within one bf16 ulp, and the ratio y_mul / y_nomul of every row is
+    that row's own routing weight (the Marlin forensic)."""
+    cfg = get_config("c0", name="ratio", T=32, E=32, k=4, H=2880, I=256)
+    L, N = make(cfg, seed=9)
+    gm = gpu_steps(L, cfg, mul=True)
+    gn = gpu_steps(L, cfg, mul=False)
+    R = cfg.T * cfg.k
+    tw = gm["topk_weights"].reshape(-1)
+    for p, row in enumerate(gm["sorted_token_ids"]):
+        if row >= R:
+            continue
+        ym, yn = gm["y"][p], gn["y"][p]
+        ext = (yn * tw[row]).astype(np.float32)
+        assert np.all(np.abs(ext - ym) <= np.abs(ym) * 2.0 ** -7 + 1e-6)
+        m = np.abs(yn) > 1e-3
+        ratio = np.median(ym[m] / yn[m])
+        assert abs(ratio - tw[row]) <= tw[row] * 2.0 ** -7
+
+
+def test_output_shape_stride_and_canary():
+    import bit_block_scaled_gb300 as moe
+    cfg = get_config("c0", name="canary", T=9, E=4, k=2, H=2880, I=128)
+    L, N = make(cfg, seed=10)
+    nbytes = moe.moe_workspace_size(cfg.T, cfg.E, cfg.k, cfg.H, cfg.I, 16)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    buf = torch.full((cfg.T * cfg.H + 4096,), -7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[:cfg.T * cfg.H].view(cfg.T, cfg.H)
+    moe.moe_forward(L["x"], L["logits"], None, cfg.k, 0, L["w13"], L["w2"], 0,
+                    moe.act("swigluoai"), 1, 16, out, ws)
+    torch.cuda.synchronize()
+    assert out.shape == (9, 2880) and out.stride() == (2880, 1)
+    assert torch.all(buf[cfg.T * cfg.H:] == -7.0)
+    o = oracle_full(N, cfg)
+    assert_close(out.float().cpu().numpy(), o["out"], "out")
+
+
+def test_empty_batch_is_a_no_op():
+    import bit_block_scaled_gb300 as moe
+    cfg = get_config("c0", name="empty", T=0, E=4, k=2, H=128, I=128)
+    L, N = make(cfg)
+    nbytes = moe.moe_workspace_size(0, 4, 2, 128, 128, 16)
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    out = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(L["x"], L["logits"], None, 2, 0, L["w13"], L["w2"], 0, moe.act(), 1, 16, out, ws)
+    assert moe.moe_last_launch_count() == 0
+    assert moe.moe_read_status(ws) == 0
+
+
+def test_bad_expert_id_latches_status():
+    import bit_block_scaled_gb300 as moe
+    T, k, E, H = 8, 2, 4, 128
+    ids = torch.tensor([[0, 1]] * T, dtype=torch.int32, device="cuda")
+    ids[3, 1] = 9                       # out of range
+    ids[5, 0] = -2
+    x = torch.randn(T, H, device="cuda").to(torch.bfloat16)
+    P = moe.moe_padded_rows(T, k, E, 16)
+    sorted_ids = torch.empty(P, dtype=torch.int32, device="cuda")
+    offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    blocks = torch.empty(P // 16, dtype=torch.int32, device="cuda")
+    row_pos = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty(P, H, dtype=torch.bfloat16, device="cuda")
+    ws = ws_status()
+    moe.moe_align_permute(ids, E, 16, x, sorted_ids, offs, blocks, row_pos, x_perm, ws)
+    st = moe.moe_read_status(ws)
+    assert st == 5, moe.moe_status_string(st)
+    rp = row_pos.cpu().numpy()
+    assert rp[3 * 2 + 1] == -1 and rp[5 * 2] == -1
+    # the valid rows are still placed
+    assert int(offs[-1]) == 32
+    moe.moe_clear_status(ws)
+    assert moe.moe_read_status(ws) == 0
+
+
+def test_invalid_arguments_rejected_on_host():
+    import bit_block_scaled_gb300 as moe
+    cfg = get_config("c0")
+    L, N = make(cfg)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(moe.moe_workspace_size(cfg.T, cfg.E, cfg.k, cfg.H, cfg.I, 16), dtype=torch.uint8,
+                     device="cuda")
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward(L["x"], L["logits"], None, cfg.k, 0, L["w13"], L["w2"], 0, moe.act(), 1, 24,
+                        out, ws)
+    assert ei.value.code == 1
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward(L["x"], L["logits"], None, cfg.k, 0, L["w13"], L["w2"], 0, moe.act(), 1, 16,
+                        out, ws[:1024])
+    assert ei.value.code == 6
+    big = torch.empty(cfg.T * cfg.H + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoeError) as ei:   # output 2 bytes off a 16-byte boundary
+        moe.moe_forward(L["x"], L["logits"], None, cfg.k, 0, L["w13"], L["w2"], 0, moe.act(), 1, 16,
+                        big[1:1 + cfg.T * cfg.H].view(cfg.T, cfg.H), ws)
+    assert ei.value.code == 1
