@@ -55,9 +55,9 @@ _SIGS = {
     "moe_grouped_gemm2_weighted": (_i32, [_vp, _vp, _vp, _i32, ctypes.POINTER(QWeight), _vp, _i32,
                                           _i32, _vp, _vp, _vp]),
     "moe_unpermute_reduce": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
-    "moe_forward": (_i32, [_vp, _vp, _vp] + [_i32] * 7 + [ctypes.POINTER(QWeight)] * 2 +
+    "moe_forward": (_i32, [_vp, _vp, _vp] + [_i32] * 6 + [ctypes.POINTER(QWeight)] * 2 +
                     [_i32, Act, _i32, _i32, _vp, _vp, _sz, _vp]),
-    "moe_forward_host": (_i32, [_vp, _vp, _vp] + [_i32] * 7 + [ctypes.POINTER(QWeight)] * 2 +
+    "moe_forward_host": (_i32, [_vp, _vp, _vp] + [_i32] * 6 + [ctypes.POINTER(QWeight)] * 2 +
                          [_i32, Act, _i32, _i32, _vp, _vp, _sz, _vp]),
     "moe_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "moe_clear_status": (_i32, [_vp, _vp]),

@@ -61,3 +61,12 @@ def test_status_strings(lib):
 def test_build_entry_point_compiles_for_sm103a():
     assert "arch=compute_103a,code=sm_103a" in " ".join(B.ARCH)
     assert os.path.exists(B.build())
+
+
+def test_binding_arity_matches_header():
+    src = open(os.path.join(ROOT, "include", "moe4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for m in re.finditer(r"\b(moe_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
+        name, args = m.group(1), m.group(2).strip()
+        n = 0 if args in ("", "void") else args.count(",") + 1
+        assert len(moe._lib._SIGS[name][1]) == n, name
