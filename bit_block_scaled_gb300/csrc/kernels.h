@@ -23,10 +23,11 @@ struct GemmArgs {
   unsigned int *status;
   int E, N, K, P_max, num_rows, ldo, layout, I, mul;
   float alpha, limit;
-  int tile_n, stages, sc_row_bytes, z_row_bytes;
+  int tile_n, stages, kpb, sc_row_bytes, z_row_bytes;
 };
 
 int choose_tile_n(int num_rows, int E);
+int choose_kpb(int tile_n);
 
 // epi: 0 = GEMM1 + swigluoai, 1 = GEMM1 + ReLU^2, 2 = GEMM2 + routing weight
 moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t *x, int P_max,
