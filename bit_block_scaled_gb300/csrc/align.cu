@@ -110,8 +110,16 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__r
   }
 }
 
-// x_perm[p] = x[sorted[p] / k], zero for padding slots; slots past the last
-// used one (offsets[E]) are never read by the GEMMs and are skipped.
+// Within every group of 8 columns, x_perm stores the elements in the order
+// 0,4,1,5,2,6,3,7 (the order the GEMM's weight expansion produces them in).
+__device__ __forceinline__ uint4 interleave8(uint4 v) {
+  return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                    __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+}
+
+// x_perm[p] = x[sorted[p] / k] (columns interleaved within groups of 8), zero
+// for padding slots; slots past the last used one (offsets[E]) are never read
+// by the GEMMs and are skipped.
 __global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x, int R, int k, int H8,
                                                      const int32_t *__restrict__ sorted,
                                                      const int32_t *__restrict__ used_end,
@@ -122,7 +130,7 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x
   uint4 *dst = x_perm + (size_t)p * H8;
   if (s >= 0 && s < R) {
     const uint4 *src = x + (size_t)(s / k) * H8;
-    for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = src[v];
+    for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = interleave8(src[v]);
   } else {
     for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
   }

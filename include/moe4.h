@@ -146,8 +146,13 @@ moe_status_t moe_route_topk(const float *logits, const float *sel_bias, int T,
  *   expert_offsets   int32 [E+1]     first slot of each expert; [E] = used slots
  *   block_expert_ids int32 [P_max/block_m]  expert of each block, -1 unused
  *   row_pos          int32 [T*k]     slot of each flat row
- *   x_perm           bf16  [P_max][H] x[sorted/k] per slot, zero in padding
- * An expert id outside [0, E) latches MOE_ERR_BAD_INDEX and is dropped. */
+ *   x_perm           bf16  [P_max][H] x[sorted/k] per slot, zero in padding,
+ *                    columns interleaved within every group of 8 (below)
+ * An expert id outside [0, E) latches MOE_ERR_BAD_INDEX and is dropped.
+ * Interleaved columns: x_perm and a_out (below) store the columns of each
+ * group of 8 in the order 0,4,1,5,2,6,3,7 -- the order in which the GEMMs
+ * expand the packed 4-bit weights -- so stored column 8g+q holds column
+ * 8g + (0,4,1,5,2,6,3,7)[q]. Only these two intermediates use it. */
 moe_status_t moe_align_permute(const int32_t *topk_ids, int T, int k, int E,
                                int block_m, const uint16_t *x, int H,
                                int32_t *sorted_token_ids, int32_t *expert_offsets,
@@ -158,6 +163,8 @@ moe_status_t moe_align_permute(const int32_t *topk_ids, int T, int k, int E,
  * NEMO]. For every used slot p of expert e (sorted_token_ids[p] < num_rows):
  *   h = (x_perm[p] . W13'[e]^T) * gscale[e] + b13[e]   (fp32 accumulate)
  *   a_out[p] = bf16(act(h))                  a_out: bf16 [P_max][I]
+ * x_perm is read and a_out written with interleaved columns (see
+ * moe_align_permute).
  * W13' is the bf16 dequantised operand. Padding slots of a_out are not written.
  * P_max must be moe_padded_rows(...) of the align call that made the metadata. */
 moe_status_t moe_grouped_gemm1_act(const uint16_t *x_perm,
@@ -172,6 +179,8 @@ moe_status_t moe_grouped_gemm1_act(const uint16_t *x_perm,
  *   z = (a[p] . W2'[e]^T) * gscale[e] + b2[e]
  *   if mul_topk_weights: z *= topk_weights_flat[sorted_token_ids[p]]
  *   y[p] = bf16(z)                            y: bf16 [P_max][H]
+ * a is read with interleaved columns (as moe_grouped_gemm1_act writes it);
+ * y has plain column order.
  * The weight is read through the slot's own flat row id (the Marlin kernel
  * read another row's entry). Padding slots of y are not written. */
 moe_status_t moe_grouped_gemm2_weighted(const uint16_t *a,

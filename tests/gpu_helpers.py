@@ -12,6 +12,25 @@ from synth import get_config, make_layer, to_numpy
 ATOL = 1e-2
 RTOL = 1e-2
 
+# x_perm and a are stored with the columns of every group of 8 interleaved:
+# stored position q holds column STORE_ORDER[q] (see include/moe4.h)
+STORE_ORDER = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+LOGICAL_POS = np.argsort(STORE_ORDER)          # column c sits at LOGICAL_POS[c]
+
+
+def deinterleave8(a):
+    a = np.asarray(a)
+    n = a.shape[-1]
+    idx = (np.arange(n) // 8) * 8 + LOGICAL_POS[np.arange(n) % 8]
+    return a[..., idx]
+
+
+def interleave8(a):
+    a = np.asarray(a)
+    n = a.shape[-1]
+    idx = (np.arange(n) // 8) * 8 + STORE_ORDER[np.arange(n) % 8]
+    return a[..., idx]
+
 
 def built():
     from bit_block_scaled_gb300 import build
@@ -59,8 +78,8 @@ def gpu_steps(L, cfg, block_m=16, layout=0, mul=True, ids=None, tw=None):
     f = lambda t: t.detach().float().cpu().numpy() if t.dtype == torch.bfloat16 else t.cpu().numpy()
     return dict(topk_ids=f(ids), topk_weights=f(tw), sorted_token_ids=f(sorted_ids)[:P],
                 expert_offsets=f(offs), block_expert_ids=f(blocks)[:P // block_m],
-                row_pos=f(row_pos)[:T * k], x_perm=f(x_perm)[:P], a=f(a)[:P], y=f(y)[:P],
-                out=f(out), status=status, P=P)
+                row_pos=f(row_pos)[:T * k], x_perm=deinterleave8(f(x_perm)[:P]),
+                a=deinterleave8(f(a)[:P]), y=f(y)[:P], out=f(out), status=status, P=P)
 
 
 def gpu_forward(L, cfg, block_m=16, layout=0, mul=True, stream=None):
@@ -123,5 +142,5 @@ def near_tie_ok(scores, got_ids, ref_ids, ulps=2):
     return bad
 
 
-__all__ = ["built", "make", "gpu_steps", "gpu_forward", "oracle_full", "assert_close", "get_config",
+__all__ = ["deinterleave8", "interleave8", "built", "make", "gpu_steps", "gpu_forward", "oracle_full", "assert_close", "get_config",
            "near_tie_ok", "OA", "OL", "OR", "ws_status", "act_of"]

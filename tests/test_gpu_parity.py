@@ -8,8 +8,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import (OR, assert_close, built, get_config, gpu_forward, gpu_steps, make,
-                         near_tie_ok, oracle_full, ws_status)
+from gpu_helpers import (OR, assert_close, built, get_config, gpu_forward, gpu_steps, interleave8,
+                         make, near_tie_ok, oracle_full, ws_status)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,7 +59,8 @@ def test_gemm2_from_oracle_intermediates():
     L, N = make(cfg)
     o = oracle_full(N, cfg)
     dev = "cuda"
-    a = torch.from_numpy(o["a"]).to(torch.bfloat16).to(dev)
+    # the library stores a with the columns of each group of 8 interleaved
+    a = torch.from_numpy(np.ascontiguousarray(interleave8(o["a"]))).to(torch.bfloat16).to(dev)
     sorted_ids = torch.from_numpy(o["sorted_token_ids"]).to(dev)
     offs = torch.from_numpy(o["expert_offsets"]).to(dev)
     tw = torch.from_numpy(o["topk_weights"].reshape(-1)).to(dev)
