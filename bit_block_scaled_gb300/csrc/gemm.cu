@@ -56,8 +56,9 @@ constexpr int kDqThreads = 256;   // warps 2..9
 constexpr int kEpiThreads = 128;  // warps 10..13
 constexpr int kTileM = 128;       // weight rows per tile (TMEM lanes)
 constexpr int kBK = 64;           // K per MMA block (128 bytes of bf16)
-constexpr int kACols = 128;       // TMEM columns for the dequantised operand:
-                                  // 128 / (32 * KPB) stage-sized buffers
+constexpr int kMinACols = 128;    // TMEM columns reserved at least for the
+                                  // dequantised operand (stage-sized buffers)
+constexpr int kMaxNA = 4;         // at most this many operand buffers
 constexpr int kMaxStagesL = 8;
 constexpr int kMaxE = 256;
 
@@ -91,11 +92,12 @@ __host__ __device__ inline Smem smem_layout(int tile_n, int stages, int kpb, int
   return s;
 }
 
-// TMEM columns: nacc accumulators of tile_n columns (rounded to 32), then
-// kACols columns of operand buffers.
+// TMEM columns: nacc accumulators of tile_n columns (rounded to 32), then the
+// operand buffers (at least kMinACols columns; whatever the power-of-two
+// allocation leaves over is used for more buffers).
 __host__ __device__ inline uint32_t tmem_acc_stride(int tile_n) { return align_up(tile_n, 32); }
 __host__ __device__ inline uint32_t tmem_need(int tile_n, int nacc) {
-  return nacc * tmem_acc_stride(tile_n) + kACols;
+  return nacc * tmem_acc_stride(tile_n) + kMinACols;
 }
 __host__ __device__ inline uint32_t tmem_cols(int tile_n, int nacc) {
   uint32_t c = 32;
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Smem L = smem_layout(p.tile_n, p.stages, KPB, p.sc_row_bytes, p.z_row_bytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int NA = kACols / (32 * KPB);  // operand buffers in TMEM
+  const int NA = p.na;                     // operand buffers in TMEM
   constexpr int kpb = KPB;                 // K blocks per pipeline stage
   constexpr uint32_t rb = 32u * KPB;       // packed bytes per weight row per stage
   const uint32_t bar0 = smem_u32(base + L.bar);
@@ -402,9 +404,12 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
           break;
         }
         tc_fence_after();
-        if (leader) {
-          const uint32_t aa = tmem + a_col + (32u * kpb) * ra.slot;
-          const uint32_t xb = x_s + rs.slot * kpb * (p.tile_n * 128);
+        // operands computed by the whole warp (warp-uniform values), issued by
+        // one elected lane
+        const uint32_t aa = tmem + a_col + (32u * kpb) * ra.slot;
+        const uint32_t xb = x_s + rs.slot * kpb * (p.tile_n * 128);
+        const uint32_t fb = afree_bar(ra.slot), eb = empty_bar(rs.slot);
+        if (elect_one()) {
 #pragma unroll
           for (int j = 0; j < kpb; ++j) {
             if (j < nkb) {
@@ -414,15 +419,16 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
                 umma_bf16_ts(acc, aa + 32u * j + 8u * kk, bd + 2u * kk, idesc, (kb0 + j + kk) != 0);
             }
           }
-          umma_commit(afree_bar(ra.slot));
-          umma_commit(empty_bar(rs.slot));
+          umma_commit(fb);
+          umma_commit(eb);
         }
         __syncwarp();
         ra.advance(NA);
         rs.advance(p.stages);
       }
       if (!ok) break;
-      if (leader) umma_commit(accfull_bar(rc.slot));
+      const uint32_t ab = accfull_bar(rc.slot);
+      if (elect_one()) umma_commit(ab);
       __syncwarp();
       rc.advance(nacc);
     }
@@ -748,9 +754,15 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   a.m_tiles = (epi == 0) ? (N / 2 + 63) / 64 : (N + kTileM - 1) / kTileM;
   a.sc_row_bytes = (w.fmt == MOE_FMT_NVFP4) ? K / 16 : (w.fmt == MOE_FMT_MXFP4 ? K / 32 : (K / 64) * 2);
   a.z_row_bytes = (w.fmt == MOE_FMT_INT4) ? (K / 64 + 1) / 2 : 0;
-  // two TMEM accumulators when they fit next to the operand buffers
+  // two TMEM accumulators when they fit next to the operand buffers; the rest
+  // of the allocation holds as many stage-sized operand buffers as fit
   a.nacc = tmem_need(a.tile_n, 2) <= 512 ? 2 : 1;
   const bool two_per_sm = tmem_cols(a.tile_n, a.nacc) <= 256;
+  {
+    const int left = (int)tmem_cols(a.tile_n, a.nacc) - a.nacc * (int)tmem_acc_stride(a.tile_n);
+    a.na = left / (32 * kpb);
+    if (a.na > kMaxNA) a.na = kMaxNA;
+  }
   // stages: as many as fit; two CTAs per SM when TMEM allows it
   const uint32_t budget = two_per_sm ? 112 * 1024 : 225 * 1024;
   int stages = kMaxStagesL;

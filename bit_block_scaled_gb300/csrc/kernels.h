@@ -23,7 +23,7 @@ struct GemmArgs {
   unsigned int *status;
   int E, N, K, P_max, num_rows, ldo, layout, I, mul;
   float alpha, limit;
-  int tile_n, stages, kpb, sc_row_bytes, z_row_bytes, m_tiles, nacc;
+  int tile_n, stages, kpb, sc_row_bytes, z_row_bytes, m_tiles, nacc, na;
 };
 
 int choose_tile_n(int num_rows, int E);
