@@ -27,7 +27,8 @@
  * Conventions for every entry point:
  *  - Device pointers are caller-owned device memory; host pointers appear only
  *    in moe_forward_host. The library never allocates memory and keeps no
- *    per-call state other than cached device properties.
+ *    per-call state other than cached device properties (and the fixed
+ *    device array that moe_forward_static uses as its workspace).
  *  - Tensors are dense, row-major, contiguous. Integers are int32. bf16 values
  *    are passed as uint16_t bit patterns. Every device pointer must be 16-byte
  *    aligned.
@@ -221,6 +222,31 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *logits_host,
                               moe_act_t act, int mul_topk_weights, int block_m,
                               uint16_t *out_host, void *ws, size_t ws_bytes,
                               moe_stream_t stream);
+
+/* The same layer with no workspace argument, for callers that cannot
+ * allocate device memory (no cudaMalloc where they run: inside a graph
+ * capture that forbids allocation, a plugin handed only its input and output
+ * buffers, a runtime whose memory budget is fixed up front). There is no
+ * counterpart on the source pages; it is a deployment convenience.
+ * The workspace is a file-scope device array of MOE_STATIC_WS_BYTES inside
+ * the library; every GPU that loads the library holds it until the process
+ * exits. Sizes whose moe_workspace_size exceeds it return
+ * MOE_ERR_UNSUPPORTED before anything is launched (at H = I = 2880, E = 32
+ * that is about 1,900 routed rows T*k).
+ * The first call on a device looks up the array's device address, so make it
+ * before any stream capture. All calls share the array: calls that overlap on
+ * the GPU race and must not be issued. Each call clears the array's status
+ * word first; status_out (device, may be NULL) receives the raw status word
+ * after the call (bit c-1 set when device error code c was detected).
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define MOE_STATIC_WS_BYTES (32u << 20)
+moe_status_t moe_forward_static(const uint16_t *x, const float *logits,
+                                const float *sel_bias, int T, int E, int k, int H,
+                                int I, int route, const moe_qweight_t *w13,
+                                const moe_qweight_t *w2, int gate_up_layout,
+                                moe_act_t act, int mul_topk_weights, int block_m,
+                                uint16_t *out, uint32_t *status_out,
+                                moe_stream_t stream);
 
 /* Reads the device status word of `ws` (synchronises `stream`); *status gets
  * the lowest-numbered latched error, or MOE_OK. */
