@@ -69,10 +69,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete; false after the
 // cycle limit (the caller latches MOE_ERR_TIMEOUT and winds down). After a few
-// quick polls the thread backs off with short sleeps, so warps that wait (the
-// producer and MMA warps are usually ahead of the dequant warps) leave the
-// issue slots to the warps doing work.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// quick polls the thread backs off with sleeps of sleep_ns between polls, so
+// waiting warps leave the issue slots to the warps doing work: waits on the
+// critical path use short sleeps, waits that normally last a whole tile long
+// ones.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t sleep_ns = 40) {
 #pragma unroll 1
   for (int i = 0; i < 4; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -80,11 +81,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i) {
-      __nanosleep(40);
+      __nanosleep(sleep_ns);
       if (mbar_try_wait(bar, parity)) return true;
     }
     if (clock64() - t0 > kWaitLimitCycles) return false;
   }
+}
+
+// Named barrier over `nthreads` threads (whole warps) that also ANDs a
+// predicate across them: every participant gets the same decision. Lets one
+// lead warp poll an mbarrier while the rest of its group blocks in hardware.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ------------------------------------------------------------------------ TMA

@@ -62,6 +62,14 @@ constexpr int kMaxNA = 4;         // at most this many operand buffers
 constexpr int kMaxStagesL = 8;
 constexpr int kMaxE = 256;
 
+// Back-off (ns) between polls of a waiting warp, per role: the MMA and
+// dequant warps wait on each other every stage (short sleeps keep the
+// hand-off fast); the producer runs ahead and the epilogue waits for a whole
+// tile, so their polls are spaced out to leave issue slots to the dequant warps.
+constexpr uint32_t kSleepProducer = 40, kSleepMma = 40, kSleepDq = 40, kSleepEpi = 40;
+// named barriers (id 0 is __syncthreads): the dequant and epilogue groups
+constexpr int kBarDq = 1, kBarEpi = 2;
+
 enum { EPI_SWIGLU = 0, EPI_RELU2 = 1, EPI_WEIGHTED = 2 };
 
 struct Smem {
@@ -323,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       const uint32_t rows1 = wrow1 < p.N ? 64 : 0;
       const int n16 = (tt.nrows + 15) & ~15;
       // block scales of this tile into scale buffer rsc.slot
-      ok = ntiles < 2 || mbar_wait(scempty_bar(rsc.slot), rsc.phase ^ 1);
+      ok = ntiles < 2 || mbar_wait(scempty_bar(rsc.slot), rsc.phase ^ 1, kSleepProducer);
       ok = __all_sync(0xffffffffu, ok && !misc[1]);
       if (!ok) {
         fail(leader);
@@ -344,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       }
       rsc.advance(2);
       for (int st = 0; st < NS; ++st) {
-        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(empty_bar(rst.slot), rst.phase ^ 1);
+        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(empty_bar(rst.slot), rst.phase ^ 1, kSleepProducer);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -388,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       const uint32_t idesc = idesc_bf16(kTileM, n16);
       const uint32_t acc = tmem + acc_stride * rc.slot;
       // the epilogue must have drained this accumulator
-      ok = ntiles < nacc || mbar_wait(accempty_bar(rc.slot), rc.phase ^ 1);
+      ok = ntiles < nacc || mbar_wait(accempty_bar(rc.slot), rc.phase ^ 1, kSleepMma);
       ok = __all_sync(0xffffffffu, ok && !misc[1]);
       if (!ok) {
         fail(leader);
@@ -397,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       for (int st = 0; st < NS; ++st) {
         const int kb0 = st * kpb;
         const int nkb = min(kpb, KB - kb0);
-        ok = mbar_wait(full_bar(rs.slot), rs.phase) && mbar_wait(dq_bar(ra.slot), ra.phase);
+        ok = mbar_wait(full_bar(rs.slot), rs.phase, kSleepMma) && mbar_wait(dq_bar(ra.slot), ra.phase, kSleepMma);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -436,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
     // ============================================================ dequant
     const int q4 = warp & 3;             // TMEM lane quarter of this warp
     const int hk = (warp >= 6) ? 1 : 0;  // which 32-wide half of each K block
+    const bool lead = warp == 2;
     const int r = q4 * 32 + lane;        // weight row in the tile == TMEM lane
     // packed / scale row in shared memory for this operand row
     const int pr = concat ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
@@ -454,20 +463,24 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       const bool row_ok = pr < 64 || wrow1 < p.N;
       const uint8_t *sc_row = base + L.sc + rsc.slot * sc_buf + (uint32_t)pr * p.sc_row_bytes;
       const uint8_t *z_row = base + L.z + rsc.slot * z_buf + (uint32_t)pr * p.z_row_bytes;
-      ok = mbar_wait(scfull_bar(rsc.slot), rsc.phase);
-      ok = __all_sync(0xffffffffu, ok && !misc[1]);
+      // the lead warp polls for the whole group; the rest block in bar.red
+      bool lok = true;
+      if (lead) lok = mbar_wait(scfull_bar(rsc.slot), rsc.phase, kSleepDq) && !misc[1];
+      ok = bar_and(kBarDq, kDqThreads, lok);
       if (!ok) {
-        fail(lane == 0);
+        fail(lead && lane == 0);
         break;
       }
       for (int st = 0; st < NS; ++st, ++kdone) {
         const int kb0 = st * kpb;
         const int nkb = min(kpb, KB - kb0);
-        ok = mbar_wait(full_bar(cs.slot), cs.phase) &&
-             (kdone < NA || mbar_wait(afree_bar(ca.slot), ca.phase ^ 1));
-        ok = __all_sync(0xffffffffu, ok && !misc[1]);
+        lok = true;
+        if (lead)
+          lok = mbar_wait(full_bar(cs.slot), cs.phase, kSleepDq) &&
+                (kdone < NA || mbar_wait(afree_bar(ca.slot), ca.phase ^ 1, kSleepDq)) && !misc[1];
+        ok = bar_and(kBarDq, kDqThreads, lok);
         if (!ok) {
-          fail(lane == 0);
+          fail(lead && lane == 0);
           break;
         }
         tc_fence_after();
@@ -580,10 +593,11 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       if (FMT == MOE_FMT_NVFP4) gmul = p.gscale[e] * 256.f;  // undo the 2^-8 operand fold
       float bias = 0.f;
       if (p.bias && col_ok) bias = bf16_bits_to_float(p.bias[(size_t)e * p.N + n_w]);
-      ok = mbar_wait(accfull_bar(rc.slot), rc.phase);
-      ok = __all_sync(0xffffffffu, ok && !misc[1]);
+      bool lok = true;
+      if (warp == 10) lok = mbar_wait(accfull_bar(rc.slot), rc.phase, kSleepEpi) && !misc[1];
+      ok = bar_and(kBarEpi, kEpiThreads, lok);
       if (!ok) {
-        fail(lane == 0);
+        fail(warp == 10 && lane == 0);
         break;
       }
       tc_fence_after();
@@ -688,7 +702,7 @@ int choose_tile_n(int num_rows, int E) {
   const int active = num_rows < E ? (num_rows > 0 ? num_rows : 1) : E;
   const int avg = (num_rows + active - 1) / active;
   int n = ((2 * avg + 15) / 16) * 16;
-  if (n < 32) n = 32;
+  if (n < 16) n = 16;
   if (n > 256) n = 256;
   return n;
 }
