@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
             if (!(r & 1) && store) {
               const float g = fminf(h, p.limit);
               const float u = fminf(fmaxf(other, -p.limit), p.limit);
-              const float sg = 1.0f / (1.0f + expf(-p.alpha * g));
+              const float sg = __fdividef(1.0f, 1.0f + __expf(-p.alpha * g));  // fast-math sigmoid
               orow[col_st] = float_to_bf16_bits((u + 1.0f) * g * sg);
             }
           } else if (EPI == EPI_RELU2) {
@@ -703,7 +703,7 @@ int choose_tile_n(int num_rows, int E) {
   const int avg = (num_rows + active - 1) / active;
   int n = ((2 * avg + 15) / 16) * 16;
   if (n < 16) n = 16;
-  if (n > 256) n = 256;
+  if (n > 128) n = 128;  // two accumulators fit TMEM next to the operand buffers
   return n;
 }
 
