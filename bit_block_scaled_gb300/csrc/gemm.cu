@@ -329,7 +329,6 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       int wrow0, wrow1;
       tile_rows(mt, wrow0, wrow1);
       const uint32_t rows1 = wrow1 < p.N ? 64 : 0;
-      const int n16 = (tt.nrows + 15) & ~15;
       // block scales of this tile into scale buffer rsc.slot
       ok = ntiles < 2 || mbar_wait(scempty_bar(rsc.slot), rsc.phase ^ 1, kSleepProducer);
       ok = __all_sync(0xffffffffu, ok && !misc[1]);
@@ -362,16 +361,15 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
           const int kb0 = st * kpb;
           const int nkb = min(kpb, KB - kb0);
           const uint32_t fb = full_bar(rst.slot);
-          mbar_arrive_expect_tx(fb, (64 + rows1) * rb + (uint32_t)(nkb * n16 * 128));
+          mbar_arrive_expect_tx(fb, (64 + rows1) * rb + (uint32_t)(nkb * p.tile_n * 128));
           const uint32_t ws = w_s + rst.slot * (kTileM * rb);
           tma_load_3d(ws, &p.tm_w, fb, st * (int)rb, wrow0, tt.e);
           if (rows1) tma_load_3d(ws + 64 * rb, &p.tm_w, fb, st * (int)rb, wrow1, tt.e);
           const uint32_t xs0 = x_s + rst.slot * xstage;
-          for (int j = 0; j < nkb; ++j) {
-            const uint32_t xs = xs0 + j * (p.tile_n * 128);
-            for (int i = 0; i < n16; i += 16)
-              tma_load_2d(xs + i * 128, &p.tm_x, fb, (kb0 + j) * kBK, tt.row0 + i);
-          }
+          // one box of tile_n token rows per K block (rows past the tile's
+          // own are loaded but never read by the MMA)
+          for (int j = 0; j < nkb; ++j)
+            tma_load_2d(xs0 + j * (p.tile_n * 128), &p.tm_x, fb, (kb0 + j) * kBK, tt.row0);
         }
         issued_mask |= 1u << rst.slot;
         issued_par = (issued_par & ~(1u << rst.slot)) | ((uint32_t)rst.phase << rst.slot);
@@ -719,6 +717,7 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   memset(&a, 0, sizeof(a));
   const int E = w.E, N = w.N, K = w.K;
   a.tile_n = choose_tile_n(num_rows, E);
+  if (a.tile_n > P_max) a.tile_n = P_max;  // the activation box never exceeds the rows (P_max % 16 == 0)
   // K blocks per pipeline stage: longer contiguous runs per weight row
   const int kpb = choose_kpb(a.tile_n);
   // packed weights: [E][N][K/2] bytes, box (32 * kpb) B x 64 rows x 1 expert
@@ -734,11 +733,11 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
       return MOE_ERR_CUDA;
   }
   a.kpb = kpb;
-  // activations: [P_max][K] bf16, box 64 x 16 rows, 128-byte swizzle
+  // activations: [P_max][K] bf16, box 64 x tile_n rows, 128-byte swizzle
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P_max};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {64, 16};
+    cuuint32_t box[2] = {64, (cuuint32_t)a.tile_n};
     cuuint32_t es[2] = {1, 1};
     if (enc(&a.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
