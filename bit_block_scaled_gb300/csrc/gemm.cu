@@ -9,20 +9,21 @@
 // into tensor memory (tcgen05.st) and the MMA reads its A operand from there,
 // while the token rows (B operand) arrive by TMA into shared memory.
 //
-// The kernel is persistent: each CTA walks the tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... and every role derives the tile coordinates by
-// itself from expert_offsets, so roles synchronise on data only. Warp roles
-// (448 threads):
-//   warp 0       TMA producer: per tile the block scales (bulk copy, two
-//                buffers), then per stage the packed 4-bit weight rows and the
-//                token rows; it runs ahead into the next tile
-//   warp 1       TMEM allocation; one lane issues tcgen05.mma (kind::f16, A
-//                from TMEM, B from shared memory) into one of two TMEM
-//                accumulators
-//   warps 2..9   dequantise: warp w owns TMEM lanes 32*(w%4).. (one weight row
-//                per lane) and half of each 64-wide K block
-//   warps 10..13 epilogue of the previous tile's accumulator while the next
-//                tile is being computed
+// The kernel is persistent, one CTA per SM (it takes all 512 TMEM columns):
+// each CTA walks the tiles blockIdx.x, blockIdx.x + gridDim.x, ... and every
+// role derives the tile coordinates by itself from expert_offsets, so roles
+// synchronise on data only. Warp roles (832 threads):
+//   warp 0        TMA producer: per tile the block scales (bulk copy, two
+//                 buffers), then per stage the packed 4-bit weight rows and
+//                 the token rows; it runs ahead into the next tile
+//   warp 1        TMEM allocation; one lane issues tcgen05.mma (kind::f16, A
+//                 from TMEM, B from shared memory) into one of two TMEM
+//                 accumulators
+//   warps 2..17   dequantise: warp w owns TMEM lanes 32*(w%4).. (one weight
+//                 row per lane) and a quarter of each stage's K range
+//   warps 18..25  epilogue of the previous tile's accumulator while the next
+//                 tile is being computed (two warps per TMEM lane quarter, one
+//                 per half of the token columns)
 // The epilogues: GEMM1 adds bias and applies swigluoai (gate/up pairs are
 // adjacent TMEM lanes) or ReLU^2; GEMM2 adds bias and multiplies each token row
 // by its own routing weight, read through that row's flat index (the failure
@@ -38,7 +39,8 @@
 //    c = 0 for MXFP4 (E8M0 exponents up to 128, i.e. scales up to 2). The
 //    scale byte -> bf16 conversion goes through a 256-entry table in shared
 //    memory.
-//  * GPTQ INT4: (q - z) * s is exact in fp32, then rounded once to bf16.
+//  * GPTQ INT4: bf16_rne((q - z) * s), the exact product rounded once, built
+//    from bf16-pair FMAs (the fp16 scale split into two bf16 parts).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -50,16 +52,17 @@ namespace moe4 {
 
 namespace {
 
-constexpr int kWarps = 14;
+constexpr int kFirstDqWarp = 2, kDqWarps = 16;
+constexpr int kFirstEpiWarp = kFirstDqWarp + kDqWarps, kEpiWarps = 8;
+constexpr int kWarps = kFirstEpiWarp + kEpiWarps;
 constexpr int kThreads = kWarps * 32;
-constexpr int kDqThreads = 256;   // warps 2..9
-constexpr int kEpiThreads = 128;  // warps 10..13
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kTileM = 128;       // weight rows per tile (TMEM lanes)
 constexpr int kBK = 64;           // K per MMA block (128 bytes of bf16)
-constexpr int kMinACols = 128;    // TMEM columns reserved at least for the
-                                  // dequantised operand (stage-sized buffers)
-constexpr int kMaxNA = 4;         // at most this many operand buffers
-constexpr int kMaxStagesL = 8;
+constexpr int kTmemCols = 512;    // the whole tensor memory of the SM
+constexpr int kMaxNA = 8;         // at most this many operand buffers
+constexpr int kMaxStagesL = 12;
 constexpr int kMaxE = 256;
 
 // Back-off (ns) between polls of a waiting warp, per role: the MMA and
@@ -91,27 +94,18 @@ __host__ __device__ inline Smem smem_layout(int tile_n, int stages, int kpb, int
   s.lut = o;  o += 256 * 4;
   s.offs = o; o += (kMaxE + 1) * 4;
   o = align_up(o, 16);
-  s.ids = o;  o += 4 * tile_n * 4;  // one copy per epilogue warp
-  s.tw = o;   o += 4 * tile_n * 4;
+  s.ids = o;  o += kEpiWarps * tile_n * 4;  // one copy per epilogue warp
+  s.tw = o;   o += kEpiWarps * tile_n * 4;
   o = align_up(o, 8);
-  s.bar = o;  o += (2 * kMaxStagesL + 2 * 4 + 8) * 8;
+  s.bar = o;  o += (2 * kMaxStagesL + 2 * kMaxNA + 8) * 8;
   s.misc = o; o += 64;
   s.total = o + 1024;  // slack for aligning the dynamic base to 1024
   return s;
 }
 
-// TMEM columns: nacc accumulators of tile_n columns (rounded to 32), then the
-// operand buffers (at least kMinACols columns; whatever the power-of-two
-// allocation leaves over is used for more buffers).
+// TMEM columns: nacc accumulators of tile_n columns (rounded to 32), then as
+// many stage-sized operand buffers as the rest of the 512 columns hold.
 __host__ __device__ inline uint32_t tmem_acc_stride(int tile_n) { return align_up(tile_n, 32); }
-__host__ __device__ inline uint32_t tmem_need(int tile_n, int nacc) {
-  return nacc * tmem_acc_stride(tile_n) + kMinACols;
-}
-__host__ __device__ inline uint32_t tmem_cols(int tile_n, int nacc) {
-  uint32_t c = 32;
-  while (c < tmem_need(tile_n, nacc)) c <<= 1;
-  return c < 256 ? 256 : c;  // >= 256 keeps at most two CTAs per SM on TMEM
-}
 
 // bf16x2 bits of (E2M1 codes) * 2^-126 for 8 packed codes c0..c7 (one K
 // group of 8) -> 4 words (c0|c4), (c1|c5), (c2|c6), (c3|c7). The activation
@@ -129,6 +123,13 @@ __device__ __forceinline__ void e2m1x8_raw(uint32_t x, uint32_t (&o)[4]) {
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(0x80008000u));
+  return d;
+}
+
+// a * b + c on bf16 pairs with a single rounding.
+__device__ __forceinline__ uint32_t bfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
@@ -218,7 +219,7 @@ __device__ __forceinline__ TokenTile find_token_tile(const int *offs, int E, int
 }  // namespace
 
 template <int FMT, int EPI, int KPB>
-__global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned start (pointer arithmetic on the shared array keeps the
   // compiler's knowledge that all these addresses are shared memory)
@@ -231,12 +232,13 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
   const uint32_t bar0 = smem_u32(base + L.bar);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStagesL + s); };
-  auto dq_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStagesL + s); };
-  auto afree_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStagesL + 4 + s); };
-  auto scfull_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStagesL + 8 + s); };
-  auto scempty_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStagesL + 10 + s); };
-  auto accfull_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStagesL + 12 + s); };
-  auto accempty_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStagesL + 14 + s); };
+  constexpr int kB2 = 2 * kMaxStagesL, kB3 = kB2 + 2 * kMaxNA;
+  auto dq_bar = [&](int s) { return bar0 + 8u * (kB2 + s); };
+  auto afree_bar = [&](int s) { return bar0 + 8u * (kB2 + kMaxNA + s); };
+  auto scfull_bar = [&](int s) { return bar0 + 8u * (kB3 + s); };
+  auto scempty_bar = [&](int s) { return bar0 + 8u * (kB3 + 2 + s); };
+  auto accfull_bar = [&](int s) { return bar0 + 8u * (kB3 + 4 + s); };
+  auto accempty_bar = [&](int s) { return bar0 + 8u * (kB3 + 6 + s); };
   volatile int *misc = reinterpret_cast<volatile int *>(base + L.misc);  // [0] tmem, [1] abort
   int *offs_s = reinterpret_cast<int *>(base + L.offs);
   int *ids_s = reinterpret_cast<int *>(base + L.ids);
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
   const int nacc = p.nacc;
   const uint32_t acc_stride = tmem_acc_stride(p.tile_n);
   const uint32_t a_col = nacc * acc_stride;
-  const uint32_t ncols = tmem_cols(p.tile_n, nacc);
+  const uint32_t ncols = kTmemCols;
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<int *>(misc)), ncols);
     tmem_relinquish();
@@ -438,11 +440,12 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       __syncwarp();
       rc.advance(nacc);
     }
-  } else if (warp < 10) {
+  } else if (warp < kFirstEpiWarp) {
     // ============================================================ dequant
-    const int q4 = warp & 3;             // TMEM lane quarter of this warp
-    const int hk = (warp >= 6) ? 1 : 0;  // which 32-wide half of each K block
-    const bool lead = warp == 2;
+    const int q4 = warp & 3;                      // TMEM lane quarter of this warp
+    const int kq = (warp - kFirstDqWarp) >> 2;    // which quarter of the stage's K
+    const bool lead = warp == kFirstDqWarp;
+    constexpr int nw = KPB / 2;                   // 32-wide K chunks per warp per stage
     const int r = q4 * 32 + lane;        // weight row in the tile == TMEM lane
     // packed / scale row in shared memory for this operand row
     const int pr = concat ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
@@ -450,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
     // the packed tile arrives with the 32/64-byte swizzle matching its row
     // width: 16-byte chunk index ^= address bits [7, 7 + log2(kpb) + 1)
     const int sw = (int)(((uint32_t)pr * rb >> 7) & (uint32_t)(2 * kpb - 1));
-    const uint32_t t_a = tmem + ((uint32_t)(q4 * 32) << 16) + a_col + 16u * hk;
+    const uint32_t t_a = tmem + ((uint32_t)(q4 * 32) << 16) + a_col;
     Ring cs, ca, rsc;
     int kdone = 0;  // K stages dequantised so far (all tiles)
     bool ok = true;
@@ -483,13 +486,15 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
         }
         tc_fence_after();
 #pragma unroll
-        for (int j = 0; j < kpb; ++j) {
+        for (int i = 0; i < nw; ++i) {
+          const int ch = kq * nw + i;  // 16-byte chunk of the row: K block ch / 2, half ch % 2
+          const int j = ch >> 1, hk = ch & 1;
           if (j < nkb) {
             const int kb = kb0 + j;
             uint32_t out[16];
             if (row_ok) {
               const uint4 c = *reinterpret_cast<const uint4 *>(w_row + cs.slot * (kTileM * rb) +
-                                                              (((2 * j + hk) ^ sw) << 4));
+                                                              ((ch ^ sw) << 4));
               const uint32_t xw[4] = {c.x, c.y, c.z, c.w};
               if (FMT == MOE_FMT_NVFP4) {
                 const uint32_t sb = *reinterpret_cast<const uint16_t *>(sc_row + kb * 4 + hk * 2);
@@ -516,18 +521,25 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
                   for (int q = 0; q < 4; ++q) out[h * 4 + q] = bmul2(o4[q], s2);
                 }
               } else {  // INT4, one group of 64 per K block
+                // bf16_rne((q - z) * s) with a single rounding, on bf16 pairs:
+                // s (fp16, 11 significant bits) = s_hi + s_lo, both exact in
+                // bf16; (q - z) * s_lo is exact in bf16 (at most 7 bits), so
+                // fma(q - z, s_hi, (q - z) * s_lo) rounds the exact product once
                 const float sf = __half2float(*reinterpret_cast<const __half *>(sc_row + kb * 2));
                 const uint32_t zz = (z_row[kb >> 1] >> ((kb & 1) * 4)) & 0xFu;
-                const float cz = -(float)zz * sf;  // exact
+                const uint32_t hi = float_to_bf16_bits(sf);
+                const uint32_t lo = float_to_bf16_bits(sf - bf16_bits_to_float((uint16_t)hi));
+                const uint32_t nz = float_to_bf16_bits(-128.f - (float)zz);  // -(128 + z), exact
+                const uint32_t shi2 = hi | (hi << 16), slo2 = lo | (lo << 16), nz2 = nz | (nz << 16);
 #pragma unroll
                 for (int w8 = 0; w8 < 4; ++w8) {
                   const uint32_t x = xw[w8];
 #pragma unroll
                   for (int q = 0; q < 4; ++q) {  // codes q and q + 4 (interleaved order)
-                    const float q0 = __uint_as_float(0x4B000000u | ((x >> (4 * q)) & 0xFu)) - 8388608.f;
-                    const float q1 = __uint_as_float(0x4B000000u | ((x >> (4 * q + 16)) & 0xFu)) - 8388608.f;
-                    const __nv_bfloat162 v = __floats2bfloat162_rn(fmaf(q0, sf, cz), fmaf(q1, sf, cz));
-                    out[w8 * 4 + q] = *reinterpret_cast<const uint32_t *>(&v);
+                    // bf16 pair (128 + code): the code sits in the low mantissa bits
+                    const uint32_t c128 = ((x >> (4 * q)) & 0x000F000Fu) | 0x43004300u;
+                    const uint32_t d = bfma2(c128, 0x3F803F80u, nz2);  // code - z, exact
+                    out[w8 * 4 + q] = bfma2(d, shi2, bmul2(d, slo2));
                   }
                 }
               }
@@ -535,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
 #pragma unroll
               for (int i = 0; i < 16; ++i) out[i] = 0u;
             }
-            tmem_st16(t_a + (32u * kpb) * ca.slot + 32u * j, out);
+            tmem_st16(t_a + (32u * kpb) * ca.slot + 32u * j + 16u * hk, out);
           }
         }
         tmem_st_wait();
@@ -551,10 +563,12 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
   } else {
     // ============================================================ epilogue
     const int q4 = warp & 3;
+    const int eh = (warp - kFirstEpiWarp) >> 2;  // which half of the token columns
+    const bool lead = warp == kFirstEpiWarp;
     const int r = q4 * 32 + lane;  // weight row in the tile == TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
-    int *ids_w = ids_s + q4 * p.tile_n;  // this warp's copy of the tile's row ids
-    float *tw_w = tw_s + q4 * p.tile_n;
+    int *ids_w = ids_s + (warp - kFirstEpiWarp) * p.tile_n;  // this warp's copy of the row ids
+    float *tw_w = tw_s + (warp - kFirstEpiWarp) * p.tile_n;
     Ring rc;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -592,15 +606,15 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       float bias = 0.f;
       if (p.bias && col_ok) bias = bf16_bits_to_float(p.bias[(size_t)e * p.N + n_w]);
       bool lok = true;
-      if (warp == 10) lok = mbar_wait(accfull_bar(rc.slot), rc.phase, kSleepEpi) && !misc[1];
+      if (lead) lok = mbar_wait(accfull_bar(rc.slot), rc.phase, kSleepEpi) && !misc[1];
       ok = bar_and(kBarEpi, kEpiThreads, lok);
       if (!ok) {
-        fail(warp == 10 && lane == 0);
+        fail(lead && lane == 0);
         break;
       }
       tc_fence_after();
       const uint32_t ta = t_lane + acc_stride * rc.slot;
-      for (int c0 = 0; c0 < n16; c0 += 16) {
+      for (int c0 = 16 * eh; c0 < n16; c0 += 32) {
         uint32_t v[16];
         tmem_ld16(ta + c0, v);
         tmem_ld_wait();
@@ -691,10 +705,10 @@ moe_status_t launch_t(const GemmArgs &a, dim3 grid, uint32_t smem, cudaStream_t 
 
 }  // namespace
 
-// Two K blocks (64 contiguous bytes per weight row) per stage for token tiles
-// up to 128 rows; one for wider tiles, whose activation rows already make each
-// stage large.
-int choose_kpb(int tile_n) { return tile_n <= 128 ? 2 : 1; }
+// K blocks per pipeline stage: four (128 contiguous bytes per weight row) for
+// the narrow token tiles of decode, whose stages are mostly weights; two for
+// wider tiles, whose activation rows already make each stage large.
+int choose_kpb(int tile_n) { return tile_n <= 32 ? 4 : 2; }
 
 int choose_tile_n(int num_rows, int E) {
   const int active = num_rows < E ? (num_rows > 0 ? num_rows : 1) : E;
@@ -726,7 +740,7 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
     cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N * (K / 2)};
     cuuint32_t box[3] = {(cuuint32_t)(32 * kpb), 64, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    const CUtensorMapSwizzle swz = kpb == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle swz = kpb == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (enc(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(w.q), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -767,29 +781,25 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   a.m_tiles = (epi == 0) ? (N / 2 + 63) / 64 : (N + kTileM - 1) / kTileM;
   a.sc_row_bytes = (w.fmt == MOE_FMT_NVFP4) ? K / 16 : (w.fmt == MOE_FMT_MXFP4 ? K / 32 : (K / 64) * 2);
   a.z_row_bytes = (w.fmt == MOE_FMT_INT4) ? (K / 64 + 1) / 2 : 0;
-  // two TMEM accumulators when they fit next to the operand buffers; the rest
-  // of the allocation holds as many stage-sized operand buffers as fit
-  a.nacc = tmem_need(a.tile_n, 2) <= 512 ? 2 : 1;
-  const bool two_per_sm = tmem_cols(a.tile_n, a.nacc) <= 256;
-  {
-    const int left = (int)tmem_cols(a.tile_n, a.nacc) - a.nacc * (int)tmem_acc_stride(a.tile_n);
-    a.na = left / (32 * kpb);
-    if (a.na > kMaxNA) a.na = kMaxNA;
-  }
-  // stages: as many as fit; two CTAs per SM when TMEM allows it
-  const uint32_t budget = two_per_sm ? 112 * 1024 : 225 * 1024;
+  // two TMEM accumulators when at least two operand buffers still fit; the
+  // rest of the 512 columns holds as many stage-sized operand buffers as fit
+  const int stride = (int)tmem_acc_stride(a.tile_n);
+  a.nacc = (2 * stride + 2 * 32 * kpb <= kTmemCols) ? 2 : 1;
+  a.na = (kTmemCols - a.nacc * stride) / (32 * kpb);
+  if (a.na > kMaxNA) a.na = kMaxNA;
+  // stages: as many as fit in shared memory
+  const uint32_t budget = 225 * 1024;
   int stages = kMaxStagesL;
   while (stages > 2 && smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes).total > budget) --stages;
   a.stages = stages;
   uint32_t smem = smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes).total;
-  // never more CTAs per SM than TMEM holds (2 x 256 or 1 x 512 columns)
-  const uint32_t min_smem = two_per_sm ? 80 * 1024 : 120 * 1024;
-  if (smem < min_smem) smem = min_smem;
+  // one CTA per SM: it allocates all of TMEM
+  if (smem < 120 * 1024) smem = 120 * 1024;
   if (smem > 227 * 1024) return MOE_ERR_UNSUPPORTED;
   // persistent grid: one wave of resident CTAs, at most one per possible tile
   const int active = num_rows < E ? num_rows : E;
   const int max_tiles = a.m_tiles * (P_max / a.tile_n + active + 1);
-  int ctas = sm_count() * (two_per_sm ? 2 : 1);
+  int ctas = sm_count();
   if (ctas > max_tiles) ctas = max_tiles;
   dim3 grid(ctas);
   if (launches) ++*launches;
@@ -800,7 +810,7 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
     if (epi == 1) return launch_t<F, EPI_RELU2, K>(a, grid, smem, stream);     \
     return launch_t<F, EPI_WEIGHTED, K>(a, grid, smem, stream);                \
   }
-#define MOE4_DISPATCH(F) MOE4_DISPATCH_K(F, 1) MOE4_DISPATCH_K(F, 2)
+#define MOE4_DISPATCH(F) MOE4_DISPATCH_K(F, 2) MOE4_DISPATCH_K(F, 4)
   MOE4_DISPATCH(MOE_FMT_NVFP4)
   MOE4_DISPATCH(MOE_FMT_MXFP4)
   MOE4_DISPATCH(MOE_FMT_INT4)

@@ -257,3 +257,43 @@ def test_invalid_arguments_rejected_on_host():
         moe.moe_forward(L["x"], L["logits"], None, cfg.k, 0, L["w13"], L["w2"], 0, moe.act(), 1, 16,
                         big[1:1 + cfg.T * cfg.H].view(cfg.T, cfg.H), ws)
     assert ei.value.code == 1
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "int4"])
+def test_dequantised_weights_bit_exact(fmt):
+    """GEMM2 with one-hot activation rows, no bias and no routing weight reads
+    single dequantised weights out of the kernel: y[p, n] = W2'[e, n, k_p]
+    (one exact product, then a bf16 value rounded to bf16 again). Every value
+    must equal the oracle's R0 operand bit for bit."""
+    import bit_block_scaled_gb300 as moe
+    from oracle import layer as OLm
+    cfg = get_config("c0", name=f"onehot_{fmt}", fmt=fmt, T=64, E=2, k=1, H=320, I=192, bias=False)
+    L, N = make(cfg, seed=11)
+    E, H, I = cfg.E, cfg.H, cfg.I
+    rows = 64
+    ks = (np.arange(rows) * 37) % I                 # column picked by each row
+    a = np.zeros((rows, I), np.float32)
+    a[np.arange(rows), ks] = 1.0
+    experts = np.arange(rows) % E
+    order = np.argsort(experts, kind="stable")      # group rows by expert
+    a, ks, experts = a[order], ks[order], experts[order]
+    offs = np.zeros(E + 1, np.int32)
+    offs[1:] = np.cumsum(np.bincount(experts, minlength=E))
+    dev = "cuda"
+    a_dev = torch.from_numpy(np.ascontiguousarray(interleave8(a))).to(torch.bfloat16).to(dev)
+    sorted_ids = torch.arange(rows, dtype=torch.int32, device=dev)
+    offs_dev = torch.from_numpy(offs).to(dev)
+    tw = torch.ones(rows, dtype=torch.float32, device=dev)
+    y = torch.zeros(rows, H, dtype=torch.bfloat16, device=dev)
+    ws = ws_status()
+    moe.moe_grouped_gemm2_weighted(a_dev, sorted_ids, offs_dev, L["w2"], tw, False, rows, y, ws)
+    assert moe.moe_read_status(ws) == 0
+    got = y.float().cpu().numpy()
+    for e in range(E):
+        W = OLm.dequant(N["w2"], e).astype(np.float32)          # [H, I]
+        gs = OLm.gscale_of(N["w2"], e)
+        for p in np.nonzero(experts == e)[0]:
+            ref = W[:, ks[p]]
+            if gs is not None:   # NVFP4: the per-expert global scale multiplies the accumulator
+                ref = OLm.bf16_rne((ref.astype(np.float32) * np.float32(gs)).astype(np.float32))
+            assert np.array_equal(got[p], ref), (fmt, e, p, np.nonzero(got[p] != ref)[0][:5])
