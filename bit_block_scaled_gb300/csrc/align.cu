@@ -3,11 +3,15 @@
 // weights", "Minimal repro": moe_align_block_size and the sorted_ids /
 // expert_ids it produces).
 //
-// align_kernel is one CTA of 1024 threads: a shared-memory expert histogram,
-// a warp prefix sum of the block-padded counts, then a stable placement of
-// the flat rows in chunks of 1024 -- the rank of a row among earlier rows of
-// the same expert comes from __match_any_sync inside a warp and a per-expert
-// prefix over the 32 warps -- so the layout does not depend on thread timing.
+// align_kernel is one CTA of 1024 threads. Warp w owns the contiguous flat rows
+// [w * R / 32, (w + 1) * R / 32) and walks them in order, 32 at a time:
+//   1. per-warp expert counts (__match_any_sync groups equal ids in a step);
+//   2. a warp prefix sum of the block-padded totals gives expert_offsets, and
+//      a per-expert prefix over the 32 warps gives each warp's first slot;
+//   3. each warp walks its rows again and places every row at its expert's
+//      running slot.
+// The order inside an expert is ascending flat row id by construction, so the
+// layout does not depend on thread timing.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,29 +28,39 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__r
                                                               int32_t *__restrict__ block_ids,
                                                               int32_t *__restrict__ row_pos,
                                                               unsigned int *status) {
-  __shared__ int cnt[kMaxE];
   __shared__ int off[kMaxE + 1];
-  __shared__ int base[kMaxE];
-  __shared__ int wcnt[32 * kMaxE];  // [warp][expert]
+  __shared__ int wcnt[32 * kMaxE];  // [warp][expert]: counts, then first slot
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r_lo = (int)((long long)R * warp / 32), r_hi = (int)((long long)R * (warp + 1) / 32);
 
-  for (int e = tid; e < E; e += kAlignThreads) cnt[e] = 0;
-  __syncthreads();
-  for (int r = tid; r < R; r += kAlignThreads) {
-    const int e = ids[r];
-    if (e < 0 || e >= E) {
-      raise_status(status, MOE_ERR_BAD_INDEX);
-      row_pos[r] = -1;
-    } else {
-      atomicAdd(&cnt[e], 1);  // integer counts: order-independent
+  // 1. per-warp counts, in row order
+  for (int e = lane; e < E; e += 32) wcnt[warp * E + e] = 0;
+  __syncwarp();
+  for (int r0 = r_lo; r0 < r_hi; r0 += 32) {
+    const int r = r0 + lane;
+    int e = -1;
+    if (r < r_hi) {
+      e = ids[r];
+      if (e < 0 || e >= E) {
+        raise_status(status, MOE_ERR_BAD_INDEX);
+        row_pos[r] = -1;
+        e = -1;
+      }
     }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+    __syncwarp();
   }
   __syncthreads();
+  // 2. expert totals -> padded offsets (warp 0), then each warp's first slot
   if (warp == 0) {
     int running = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      const int pc = (e < E) ? (cnt[e] + bm - 1) / bm * bm : 0;
+      int c = 0;
+      if (e < E)
+        for (int w = 0; w < 32; ++w) c += wcnt[w * E + e];
+      const int pc = (c + bm - 1) / bm * bm;
       int incl = pc;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -59,8 +73,15 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__r
     if (lane == 0) off[E] = running;
   }
   __syncthreads();
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int run = off[e];
+    for (int w = 0; w < 32; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+  }
   for (int e = tid; e <= E; e += kAlignThreads) offsets[e] = off[e];
-  for (int e = tid; e < E; e += kAlignThreads) base[e] = off[e];
   for (int q = tid; q < P_max; q += kAlignThreads) sorted[q] = R;
   const int nb = P_max / bm;
   for (int b = tid; b < nb; b += kAlignThreads) {
@@ -77,36 +98,23 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__r
     block_ids[b] = be;
   }
   __syncthreads();
-
-  for (int c0 = 0; c0 < R; c0 += kAlignThreads) {
-    const int r = c0 + tid;
+  // 3. placement, in row order within each warp
+  for (int r0 = r_lo; r0 < r_hi; r0 += 32) {
+    const int r = r0 + lane;
     int e = -1;
-    if (r < R) {
+    if (r < r_hi) {
       e = ids[r];
       if (e < 0 || e >= E) e = -1;
     }
-    for (int i = tid; i < 32 * E; i += kAlignThreads) wcnt[i] = 0;
-    __syncthreads();
     const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
-    __syncthreads();
-    for (int e2 = tid; e2 < E; e2 += kAlignThreads) {
-      int run = base[e2];
-      for (int w = 0; w < 32; ++w) {
-        const int c = wcnt[w * E + e2];
-        wcnt[w * E + e2] = run;
-        run += c;
-      }
-      base[e2] = run;
-    }
-    __syncthreads();
     if (e >= 0) {
-      const int pos = wcnt[warp * E + e] + rank;
+      const int pos = wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
       sorted[pos] = r;
       row_pos[r] = pos;
     }
-    __syncthreads();
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+    __syncwarp();
   }
 }
 

@@ -68,22 +68,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete; false after the
-// cycle limit (the caller latches MOE_ERR_TIMEOUT and winds down). After a few
-// quick polls the thread backs off with sleeps of sleep_ns between polls, so
-// waiting warps leave the issue slots to the warps doing work: waits on the
-// critical path use short sleeps, waits that normally last a whole tile long
-// ones.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t sleep_ns = 40) {
-#pragma unroll 1
-  for (int i = 0; i < 4; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+// cycle limit (the caller latches MOE_ERR_TIMEOUT and winds down). try_wait
+// itself parks the thread for a short, hardware-chosen time when the phase is
+// still open, so a plain retry loop keeps the hand-off latency low without
+// flooding the issue slots (only one warp of each group polls).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i) {
-      __nanosleep(sleep_ns);
+    for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    }
     if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }

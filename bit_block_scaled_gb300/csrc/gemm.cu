@@ -65,11 +65,6 @@ constexpr int kMaxNA = 8;         // at most this many operand buffers
 constexpr int kMaxStagesL = 12;
 constexpr int kMaxE = 256;
 
-// Back-off (ns) between polls of a waiting warp, per role: the MMA and
-// dequant warps wait on each other every stage (short sleeps keep the
-// hand-off fast); the producer runs ahead and the epilogue waits for a whole
-// tile, so their polls are spaced out to leave issue slots to the dequant warps.
-constexpr uint32_t kSleepProducer = 40, kSleepMma = 40, kSleepDq = 40, kSleepEpi = 40;
 // named barriers (id 0 is __syncthreads): the dequant and epilogue groups
 constexpr int kBarDq = 1, kBarEpi = 2;
 
@@ -332,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       tile_rows(mt, wrow0, wrow1);
       const uint32_t rows1 = wrow1 < p.N ? 64 : 0;
       // block scales of this tile into scale buffer rsc.slot
-      ok = ntiles < 2 || mbar_wait(scempty_bar(rsc.slot), rsc.phase ^ 1, kSleepProducer);
+      ok = ntiles < 2 || mbar_wait(scempty_bar(rsc.slot), rsc.phase ^ 1);
       ok = __all_sync(0xffffffffu, ok && !misc[1]);
       if (!ok) {
         fail(leader);
@@ -353,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       }
       rsc.advance(2);
       for (int st = 0; st < NS; ++st) {
-        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(empty_bar(rst.slot), rst.phase ^ 1, kSleepProducer);
+        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(empty_bar(rst.slot), rst.phase ^ 1);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -396,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       const uint32_t idesc = idesc_bf16(kTileM, n16);
       const uint32_t acc = tmem + acc_stride * rc.slot;
       // the epilogue must have drained this accumulator
-      ok = ntiles < nacc || mbar_wait(accempty_bar(rc.slot), rc.phase ^ 1, kSleepMma);
+      ok = ntiles < nacc || mbar_wait(accempty_bar(rc.slot), rc.phase ^ 1);
       ok = __all_sync(0xffffffffu, ok && !misc[1]);
       if (!ok) {
         fail(leader);
@@ -405,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       for (int st = 0; st < NS; ++st) {
         const int kb0 = st * kpb;
         const int nkb = min(kpb, KB - kb0);
-        ok = mbar_wait(full_bar(rs.slot), rs.phase, kSleepMma) && mbar_wait(dq_bar(ra.slot), ra.phase, kSleepMma);
+        ok = mbar_wait(full_bar(rs.slot), rs.phase) && mbar_wait(dq_bar(ra.slot), ra.phase);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -466,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       const uint8_t *z_row = base + L.z + rsc.slot * z_buf + (uint32_t)pr * p.z_row_bytes;
       // the lead warp polls for the whole group; the rest block in bar.red
       bool lok = true;
-      if (lead) lok = mbar_wait(scfull_bar(rsc.slot), rsc.phase, kSleepDq) && !misc[1];
+      if (lead) lok = mbar_wait(scfull_bar(rsc.slot), rsc.phase) && !misc[1];
       ok = bar_and(kBarDq, kDqThreads, lok);
       if (!ok) {
         fail(lead && lane == 0);
@@ -477,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int nkb = min(kpb, KB - kb0);
         lok = true;
         if (lead)
-          lok = mbar_wait(full_bar(cs.slot), cs.phase, kSleepDq) &&
-                (kdone < NA || mbar_wait(afree_bar(ca.slot), ca.phase ^ 1, kSleepDq)) && !misc[1];
+          lok = mbar_wait(full_bar(cs.slot), cs.phase) &&
+                (kdone < NA || mbar_wait(afree_bar(ca.slot), ca.phase ^ 1)) && !misc[1];
         ok = bar_and(kBarDq, kDqThreads, lok);
         if (!ok) {
           fail(lead && lane == 0);
@@ -606,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       float bias = 0.f;
       if (p.bias && col_ok) bias = bf16_bits_to_float(p.bias[(size_t)e * p.N + n_w]);
       bool lok = true;
-      if (lead) lok = mbar_wait(accfull_bar(rc.slot), rc.phase, kSleepEpi) && !misc[1];
+      if (lead) lok = mbar_wait(accfull_bar(rc.slot), rc.phase) && !misc[1];
       ok = bar_and(kBarEpi, kEpiThreads, lok);
       if (!ok) {
         fail(lead && lane == 0);

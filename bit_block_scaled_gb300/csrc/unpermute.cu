@@ -20,10 +20,14 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4 v) {
   }
 }
 
-__global__ void __launch_bounds__(128) unpermute_kernel(const uint4 *__restrict__ y,
-                                                        const int32_t *__restrict__ row_pos, int T, int k,
-                                                        int H8, int P_max, uint4 *__restrict__ out,
-                                                        unsigned int *status) {
+constexpr int kUnpermThreads = 64;  // one 8-column vector per thread
+
+// grid (T, ceil(H/8 / 64)): each CTA covers 512 columns of one token, so even
+// a small batch spreads over many SMs
+__global__ void __launch_bounds__(kUnpermThreads) unpermute_kernel(const uint4 *__restrict__ y,
+                                                                   const int32_t *__restrict__ row_pos, int T,
+                                                                   int k, int H8, int P_max,
+                                                                   uint4 *__restrict__ out, unsigned int *status) {
   const int t = blockIdx.x;
   int pos[8];
   bool ok = true;
@@ -35,8 +39,9 @@ __global__ void __launch_bounds__(128) unpermute_kernel(const uint4 *__restrict_
       if (pos[j] < 0 || pos[j] >= P_max) ok = false;
     }
   }
-  if (!ok && threadIdx.x == 0) raise_status(status, MOE_ERR_BAD_INDEX);
-  for (int v = threadIdx.x; v < H8; v += blockDim.x) {
+  if (!ok && threadIdx.x == 0 && blockIdx.y == 0) raise_status(status, MOE_ERR_BAD_INDEX);
+  const int v = blockIdx.y * kUnpermThreads + threadIdx.x;
+  if (v < H8) {
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -56,8 +61,10 @@ __global__ void __launch_bounds__(128) unpermute_kernel(const uint4 *__restrict_
 moe_status_t launch_unpermute(const uint16_t *y, const int32_t *row_pos, int T, int k, int H, int P_max,
                               uint16_t *out, unsigned int *status, cudaStream_t stream, int *launches) {
   if (T == 0) return MOE_OK;
-  unpermute_kernel<<<T, 128, 0, stream>>>(reinterpret_cast<const uint4 *>(y), row_pos, T, k, H / 8, P_max,
-                                          reinterpret_cast<uint4 *>(out), status);
+  const int H8 = H / 8;
+  const dim3 grid(T, (H8 + kUnpermThreads - 1) / kUnpermThreads);
+  unpermute_kernel<<<grid, kUnpermThreads, 0, stream>>>(reinterpret_cast<const uint4 *>(y), row_pos, T, k, H8,
+                                                        P_max, reinterpret_cast<uint4 *>(out), status);
   if (launches) ++*launches;
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
