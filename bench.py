@@ -62,9 +62,19 @@ def read_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def gemm_source_hash():
+    """Hash of the GEMM kernel sources, recorded beside each ncu summary."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "bit_block_scaled_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def read_traffic(kernel_tag):
     """DRAM bytes per launch of the kernel from the committed ncu summary, if
-    it was captured for the current kernel source."""
+    it was captured for the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.txt")
     try:
         vals = {}
@@ -73,6 +83,8 @@ def read_traffic(kernel_tag):
                 if ":" in line:
                     k, v = line.split(":", 1)
                     vals[k.strip()] = v.strip()
+        if vals.get("source_hash") != gemm_source_hash():
+            return None, vals.get("source_hash")
         return float(vals["traffic_bytes_per_launch"]), vals.get("source_hash")
     except Exception:
         return None, None
