@@ -19,8 +19,9 @@
 //   warp 1        TMEM allocation; one lane issues tcgen05.mma (kind::f16, A
 //                 from TMEM, B from shared memory) into one of two TMEM
 //                 accumulators
-//   warps 2..17   dequantise: warp w owns TMEM lanes 32*(w%4).. (one weight
-//                 row per lane) and a quarter of each stage's K range
+//   warps 2..17   dequantise, in two groups of 8 that take alternate stages:
+//                 warp w owns TMEM lanes 32*(w%4).. (one weight row per lane)
+//                 and half of its group's stage K range
 //   warps 18..25  epilogue of the previous tile's accumulator while the next
 //                 tile is being computed (two warps per TMEM lane quarter, one
 //                 per half of the token columns)
@@ -57,6 +58,7 @@ constexpr int kFirstEpiWarp = kFirstDqWarp + kDqWarps, kEpiWarps = 8;
 constexpr int kWarps = kFirstEpiWarp + kEpiWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kDqGroupThreads = kDqThreads / 2;  // one of the two dequant groups
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kTileM = 128;       // weight rows per tile (TMEM lanes)
 constexpr int kBK = 64;           // K per MMA block (128 bytes of bf16)
@@ -66,7 +68,7 @@ constexpr int kMaxStagesL = 12;
 constexpr int kMaxE = 256;
 
 // named barriers (id 0 is __syncthreads): the dequant and epilogue groups
-constexpr int kBarDq = 1, kBarEpi = 2;
+constexpr int kBarDq0 = 1, kBarEpi = 2, kBarDq1 = 3;
 
 enum { EPI_SWIGLU = 0, EPI_RELU2 = 1, EPI_WEIGHTED = 2 };
 
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(empty_bar(s), 1);
     }
     for (int s = 0; s < NA; ++s) {
-      mbar_init(dq_bar(s), kDqThreads);
+      mbar_init(dq_bar(s), kDqGroupThreads);
       mbar_init(afree_bar(s), 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -437,10 +439,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   } else if (warp < kFirstEpiWarp) {
     // ============================================================ dequant
+    // Two groups of 8 warps take alternate K stages, so one group's barrier
+    // waits overlap the other group's arithmetic. In a group, warp w owns TMEM
+    // lane quarter w % 4 and one half of the stage's K range.
+    const int dw = warp - kFirstDqWarp;
+    const int grp = dw >> 3;                      // 0: even stages, 1: odd stages
     const int q4 = warp & 3;                      // TMEM lane quarter of this warp
-    const int kq = (warp - kFirstDqWarp) >> 2;    // which quarter of the stage's K
-    const bool lead = warp == kFirstDqWarp;
-    constexpr int nw = KPB / 2;                   // 32-wide K chunks per warp per stage
+    const int kq = (dw >> 2) & 1;                 // which half of the stage's K
+    const bool lead = (dw & 7) == 0;              // polls the barriers for its group
+    const int gbar = grp ? kBarDq1 : kBarDq0;
+    constexpr int nw = KPB;                       // 32-wide K chunks per warp per stage
     const int r = q4 * 32 + lane;        // weight row in the tile == TMEM lane
     // packed / scale row in shared memory for this operand row
     const int pr = concat ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
@@ -462,19 +470,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       // the lead warp polls for the whole group; the rest block in bar.red
       bool lok = true;
       if (lead) lok = mbar_wait(scfull_bar(rsc.slot), rsc.phase) && !misc[1];
-      ok = bar_and(kBarDq, kDqThreads, lok);
+      ok = bar_and(gbar, kDqGroupThreads, lok);
       if (!ok) {
         fail(lead && lane == 0);
         break;
       }
       for (int st = 0; st < NS; ++st, ++kdone) {
+        if ((kdone & 1) != grp) {  // the other group's stage
+          ca.advance(NA);
+          cs.advance(p.stages);
+          continue;
+        }
         const int kb0 = st * kpb;
         const int nkb = min(kpb, KB - kb0);
         lok = true;
         if (lead)
           lok = mbar_wait(full_bar(cs.slot), cs.phase) &&
                 (kdone < NA || mbar_wait(afree_bar(ca.slot), ca.phase ^ 1)) && !misc[1];
-        ok = bar_and(kBarDq, kDqThreads, lok);
+        ok = bar_and(gbar, kDqGroupThreads, lok);
         if (!ok) {
           fail(lead && lane == 0);
           break;
