@@ -723,7 +723,10 @@ int choose_tile_n(int num_rows, int E) {
   const int avg = (num_rows + active - 1) / active;
   int n = ((2 * avg + 15) / 16) * 16;
   if (n < 16) n = 16;
-  if (n > 128) n = 128;  // two accumulators fit TMEM next to the operand buffers
+  // wider tiles amortise each dequantised weight tile over more tokens; 192
+  // rows (two accumulators still fit TMEM next to two operand buffers) only
+  // when the experts are full enough to fill them
+  if (n > 128) n = avg >= 160 ? 192 : 128;
   return n;
 }
 
