@@ -154,6 +154,22 @@ def rejected(clocks):
     return bool(sm and mx and sm < 0.5 * mx and not clocks.get("reasons"))
 
 
+def reduce_max_over_ranks(pg, values, device):
+    """Max over ranks of each per-rank duration: the slowest replica sets the
+    job's time. pg is torch.distributed (initialised) or None for one rank."""
+    import torch
+    if pg is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_tokens_per_s(world, tokens_per_step, steps, total_ms):
+    """Whole-job throughput: every replica processes tokens_per_step per step."""
+    return world * tokens_per_step * steps / (total_ms / 1e3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -275,18 +291,13 @@ def run_ours(args):
         e_ev.synchronize()
         e2e_times.append(s_ev.elapsed_time(e_ev))
 
-    if pg:
-        t = torch.tensor([total_ms, sum(e2e_times)], device="cuda", dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms, e2e_total = float(t[0]), float(t[1])
-    else:
-        e2e_total = sum(e2e_times)
+    total_ms, e2e_total = reduce_max_over_ranks(pg, [total_ms, sum(e2e_times)], "cuda")
     if rank != 0:
         if pg:
             pg.destroy_process_group()
         return
     ms = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1e3)
+    value = job_tokens_per_s(world, T, args.steps, total_ms)
     e2e_ms = e2e_total / len(e2e_times)
     ids = None
     try:
@@ -343,7 +354,7 @@ def run_ours(args):
         "algorithmic_flops": int(flops),
         "breakdown_ms": {k2: round(v, 5) for k2, v in bd.items()},
         "roofline": roofline,
-        "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(world, T, 1, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": int(T * H * 2 + T * E * 4), "d2h_bytes_per_step": int(T * H * 2)},
         "gpu_launches": int(launches_per_step * args.steps),
