@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__r
                                                               unsigned int *status) {
   __shared__ int off[kMaxE + 1];
   __shared__ int wcnt[32 * kMaxE];  // [warp][expert]: counts, then first slot
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r_lo = (int)((long long)R * warp / 32), r_hi = (int)((long long)R * (warp + 1) / 32);
 
@@ -132,6 +134,8 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x
                                                      const int32_t *__restrict__ sorted,
                                                      const int32_t *__restrict__ used_end,
                                                      uint4 *__restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
   const int p = blockIdx.x;
   if (p >= *used_end) return;
   const int s = sorted[p];
@@ -149,19 +153,20 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x
 moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, int P_max,
                           int32_t *sorted_ids, int32_t *offsets, int32_t *block_ids, int32_t *row_pos,
                           unsigned int *status, cudaStream_t stream, int *launches) {
-  align_kernel<<<1, kAlignThreads, 0, stream>>>(ids, T * k, E, block_m, P_max, sorted_ids, offsets, block_ids,
-                                                row_pos, status);
+  const cudaError_t err = launch_pdl(align_kernel, dim3(1), dim3(kAlignThreads), 0, stream, ids, T * k, E, block_m,
+                                     P_max, sorted_ids, offsets, block_ids, row_pos, status);
   if (launches) ++*launches;
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
                            const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches) {
   if (P_max == 0) return MOE_OK;
-  gather_kernel<<<P_max, 128, 0, stream>>>(reinterpret_cast<const uint4 *>(x), T * k, k, H / 8, sorted_ids,
-                                           offsets_end, reinterpret_cast<uint4 *>(x_perm));
+  const cudaError_t err = launch_pdl(gather_kernel, dim3(P_max), dim3(128), 0, stream,
+                                     reinterpret_cast<const uint4 *>(x), T * k, k, H / 8, sorted_ids, offsets_end,
+                                     reinterpret_cast<uint4 *>(x_perm));
   if (launches) ++*launches;
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe4

@@ -11,7 +11,34 @@
 
 #include "../../include/moe4.h"
 
+#include <utility>
+
 namespace moe4 {
+
+// ------------------------------------------------ programmatic dependent launch
+// Kernels are launched with programmatic stream serialisation: the next kernel
+// on the stream may be scheduled (and run its setup) while this one drains.
+// pdl_wait() blocks until the preceding kernel has completed and its writes
+// are visible, so every kernel calls it before reading anything a preceding
+// kernel produced; pdl_trigger() lets the following kernel be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- status bits
 // Bit (code - 1) of the device status word is set when a kernel detects code.

@@ -245,12 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   const uint32_t z_buf = align_up(kTileM * p.z_row_bytes, 128);
 
   // ------------------------------------------------------------------ setup
-  for (int i = tid; i <= p.E; i += kThreads) {
-    const int v = p.expert_offsets[i];
-    const bool good = v >= 0 && v <= p.P_max;
-    offs_s[i] = good ? v : 0;
-    if (!good) raise_status(p.status, MOE_ERR_BAD_INDEX);
-  }
   if (tid < 256) {
     if (FMT == MOE_FMT_NVFP4) lut[tid] = e4m3_times_2p118_x2((uint32_t)tid);
     if (FMT == MOE_FMT_MXFP4) lut[tid] = e8m0_times_2p126_x2((uint32_t)tid);
@@ -280,6 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<int *>(misc)), ncols);
     tmem_relinquish();
+  }
+  // everything above overlaps the previous kernel; its outputs are read below
+  pdl_wait();
+  pdl_trigger();
+  for (int i = tid; i <= p.E; i += kThreads) {
+    const int v = p.expert_offsets[i];
+    const bool good = v >= 0 && v <= p.P_max;
+    offs_s[i] = good ? v : 0;
+    if (!good) raise_status(p.status, MOE_ERR_BAD_INDEX);
   }
   tc_fence_before();
   __syncthreads();
@@ -707,8 +710,7 @@ moe_status_t launch_t(const GemmArgs &a, dim3 grid, uint32_t smem, cudaStream_t 
       return MOE_ERR_CUDA;
     configured = smem;
   }
-  kern<<<grid, kThreads, smem, st>>>(a);
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_pdl(kern, grid, dim3(kThreads), smem, st, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace

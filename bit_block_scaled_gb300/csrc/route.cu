@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restr
                                                             const float *__restrict__ sel_bias, int T, int E,
                                                             int k, int32_t *__restrict__ ids,
                                                             float *__restrict__ weights) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -104,12 +106,14 @@ moe_status_t launch_route(const float *logits, const float *sel_bias, int T, int
   (void)status;
   if (T == 0) return MOE_OK;
   const dim3 grid((T + kWarps - 1) / kWarps), block(kWarps * 32);
-  if (route == MOE_ROUTE_SIGMOID_BIAS)
-    route_kernel<MOE_ROUTE_SIGMOID_BIAS><<<grid, block, 0, stream>>>(logits, sel_bias, T, E, k, ids, weights);
-  else
-    route_kernel<MOE_ROUTE_TOPK_SOFTMAX><<<grid, block, 0, stream>>>(logits, sel_bias, T, E, k, ids, weights);
+  const cudaError_t err =
+      route == MOE_ROUTE_SIGMOID_BIAS
+          ? launch_pdl(route_kernel<MOE_ROUTE_SIGMOID_BIAS>, grid, block, 0, stream, logits, sel_bias, T, E, k, ids,
+                       weights)
+          : launch_pdl(route_kernel<MOE_ROUTE_TOPK_SOFTMAX>, grid, block, 0, stream, logits, sel_bias, T, E, k, ids,
+                       weights);
   if (launches) ++*launches;
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe4

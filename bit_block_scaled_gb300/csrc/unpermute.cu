@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kUnpermThreads) unpermute_kernel(const uint4 *
                                                                    const int32_t *__restrict__ row_pos, int T,
                                                                    int k, int H8, int P_max,
                                                                    uint4 *__restrict__ out, unsigned int *status) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   int pos[8];
   bool ok = true;
@@ -63,10 +65,11 @@ moe_status_t launch_unpermute(const uint16_t *y, const int32_t *row_pos, int T, 
   if (T == 0) return MOE_OK;
   const int H8 = H / 8;
   const dim3 grid(T, (H8 + kUnpermThreads - 1) / kUnpermThreads);
-  unpermute_kernel<<<grid, kUnpermThreads, 0, stream>>>(reinterpret_cast<const uint4 *>(y), row_pos, T, k, H8,
-                                                        P_max, reinterpret_cast<uint4 *>(out), status);
+  const cudaError_t err = launch_pdl(unpermute_kernel, grid, dim3(kUnpermThreads), 0, stream,
+                                     reinterpret_cast<const uint4 *>(y), row_pos, T, k, H8, P_max,
+                                     reinterpret_cast<uint4 *>(out), status);
   if (launches) ++*launches;
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe4
