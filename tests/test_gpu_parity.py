@@ -297,3 +297,22 @@ def test_dequantised_weights_bit_exact(fmt):
             if gs is not None:   # NVFP4: the per-expert global scale multiplies the accumulator
                 ref = OLm.bf16_rne((ref.astype(np.float32) * np.float32(gs)).astype(np.float32))
             assert np.array_equal(got[p], ref), (fmt, e, p, np.nonzero(got[p] != ref)[0][:5])
+
+
+# few routed rows spread over many experts (mostly one or two rows per
+# expert): narrow token tiles, many experts with no rows at all
+SMALL = [
+    # fmt, act, H, I, E, T, k, layout
+    ("nvfp4", "swigluoai", 320, 192, 32, 3, 2, 0),
+    ("nvfp4", "swigluoai", 320, 192, 32, 3, 2, 1),
+    ("nvfp4", "relu2", 192, 320, 24, 5, 3, 0),
+    ("mxfp4", "swigluoai", 384, 256, 64, 1, 4, 0),
+    ("mxfp4", "relu2", 256, 192, 16, 4, 2, 0),
+    ("int4", "swigluoai", 320, 256, 40, 6, 4, 0),
+    ("int4", "relu2", 448, 192, 20, 2, 3, 0),
+]
+
+
+@pytest.mark.parametrize("fmt,act,H,I,E,T,k,layout", SMALL)
+def test_small_batch_many_experts(fmt, act, H, I, E, T, k, layout):
+    test_formats_and_activations(fmt, act, H, I, E, T, k, layout)
