@@ -368,48 +368,28 @@ def run_ours(args):
 
 
 def breakdown(moe, L, cfg, bm, stream, flush, iters):
-    """Median duration of each step entry point (flushed L2 before each pass)."""
+    """Median device time of each of moe_forward's six kernels, as the forward
+    runs them (moe_forward_profile: CUDA events around each launch on the
+    stream; L2 flushed before each pass)."""
     import torch
     T, E, k, H, I = cfg.T, cfg.E, cfg.k, cfg.H, cfg.I
-    dev = "cuda"
-    P = moe.moe_padded_rows(T, k, E, bm)
-    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
-    tw = torch.empty(T, k, dtype=torch.float32, device=dev)
-    srt = torch.empty(P, dtype=torch.int32, device=dev)
-    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    blk = torch.empty(P // bm, dtype=torch.int32, device=dev)
-    rp = torch.empty(T * k, dtype=torch.int32, device=dev)
-    xp = torch.empty(P, H, dtype=torch.bfloat16, device=dev)
-    a = torch.empty(P, I, dtype=torch.bfloat16, device=dev)
-    y = torch.empty(P, H, dtype=torch.bfloat16, device=dev)
-    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(moe.moe_workspace_size(T, E, k, H, I, bm), dtype=torch.uint8, device="cuda")
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     act = moe.act(cfg.act, cfg.alpha, cfg.limit)
     q13, q2 = moe.qweight(L["w13"]), moe.qweight(L["w2"])
     route = moe.ROUTE[cfg.route]
-    steps = [
-        ("route_ms", lambda: moe.moe_route_topk(L["logits"], L["sel_bias"], k, route, ids, tw, ws, stream)),
-        ("align_gather_ms", lambda: moe.moe_align_permute(ids, E, bm, L["x"], srt, offs, blk, rp, xp, ws,
-                                                          stream)),
-        ("gemm1_ms", lambda: moe.moe_grouped_gemm1_act(xp, srt, offs, T * k, q13, 0, act, a, ws, stream)),
-        ("gemm2_ms", lambda: moe.moe_grouped_gemm2_weighted(a, srt, offs, q2, tw.view(-1), 1, T * k, y, ws,
-                                                            stream)),
-        ("unpermute_ms", lambda: moe.moe_unpermute_reduce(y, rp, T, k, out, ws, stream)),
-    ]
-    res = {name: [] for name, _ in steps}
+    res = {}
     with torch.cuda.stream(stream):
         for it in range(iters + 3):
             flush.zero_()
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(steps) + 1)]
-            evs[0].record(stream)
-            for i, (_, fn) in enumerate(steps):
-                fn()
-                evs[i + 1].record(stream)
-            torch.cuda.synchronize()
+            ms = moe.moe_forward_profile(L["x"], L["logits"], L["sel_bias"], k, route, q13, q2, 0, act, 1, bm,
+                                         out, ws, stream)
             if it >= 3:
-                for i, (name, _) in enumerate(steps):
-                    res[name].append(evs[i].elapsed_time(evs[i + 1]))
-    return {name: statistics.median(v) for name, v in res.items()}
+                for name, v in ms.items():
+                    res.setdefault(name, []).append(v)
+    med = {name: statistics.median(v) for name, v in res.items()}
+    return {"route_ms": med["route"], "align_gather_ms": med["align"] + med["gather"],
+            "gemm1_ms": med["gemm1"], "gemm2_ms": med["gemm2"], "unpermute_ms": med["unpermute"]}
 
 
 # ---------------------------------------------------------- the CPU oracle

@@ -24,7 +24,7 @@ STATUS_BYTES = 256
 EXPORTS = ("moe_padded_rows", "moe_workspace_size", "moe_route_topk", "moe_align_permute",
            "moe_grouped_gemm1_act", "moe_grouped_gemm2_weighted", "moe_unpermute_reduce",
            "moe_forward", "moe_forward_host", "moe_read_status", "moe_clear_status",
-           "moe_status_string", "moe_last_launch_count", "moe_forward_static")
+           "moe_status_string", "moe_last_launch_count", "moe_forward_static", "moe_forward_profile")
 
 
 class MoeError(RuntimeError):
@@ -59,6 +59,8 @@ _SIGS = {
                     [_i32, Act, _i32, _i32, _vp, _vp, _sz, _vp]),
     "moe_forward_host": (_i32, [_vp, _vp, _vp] + [_i32] * 6 + [ctypes.POINTER(QWeight)] * 2 +
                          [_i32, Act, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "moe_forward_profile": (_i32, [_vp, _vp, _vp] + [_i32] * 6 + [ctypes.POINTER(QWeight)] * 2 +
+                            [_i32, Act, _i32, _i32, _vp, _vp, _sz, _vp, _vp]),
     "moe_forward_static": (_i32, [_vp, _vp, _vp] + [_i32] * 6 + [ctypes.POINTER(QWeight)] * 2 +
                            [_i32, Act, _i32, _i32, _vp, _vp, _vp]),
     "moe_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
@@ -190,6 +192,22 @@ def moe_forward_host(x_host, logits_host, sel_bias, k, route, w13, w2, gate_up_l
                                    route, ctypes.byref(q13), ctypes.byref(q2), gate_up_layout,
                                    activation, int(mul_topk_weights), block_m, _ptr(out_host),
                                    _ptr(ws), ws.numel(), _stream(stream)), "moe_forward_host")
+
+
+def moe_forward_profile(x, logits, sel_bias, k, route, w13, w2, gate_up_layout, activation,
+                        mul_topk_weights, block_m, out, ws, stream=None):
+    """moe_forward plus the device time (ms) of its six kernels:
+    dict(route, align, gather, gemm1, gemm2, unpermute)."""
+    T, H = x.shape
+    E = logits.shape[1]
+    q13 = w13 if isinstance(w13, QWeight) else qweight(w13)
+    q2 = w2 if isinstance(w2, QWeight) else qweight(w2)
+    ms = (ctypes.c_float * 6)()
+    _check(load().moe_forward_profile(_ptr(x), _ptr(logits), _ptr(sel_bias), T, E, k, H, q2.K, route,
+                                      ctypes.byref(q13), ctypes.byref(q2), gate_up_layout, activation,
+                                      int(mul_topk_weights), block_m, _ptr(out), _ptr(ws), ws.numel(),
+                                      _stream(stream), ms), "moe_forward_profile")
+    return dict(zip(("route", "align", "gather", "gemm1", "gemm2", "unpermute"), list(ms)))
 
 
 def moe_forward_static(x, logits, sel_bias, k, route, w13, w2, gate_up_layout, activation,

@@ -148,7 +148,74 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x
   }
 }
 
+// f16 operand path: x16[p] = f16(x[sorted[p] / k] * 2^-e_p) in natural column
+// order, where e_p >= 0 is the smallest exponent that brings the row's largest
+// magnitude to at most 2^15, so every element fits f16 (the scaling is exact;
+// only elements below 2^-24 of the scaled row lose bits). xexp[p] = e_p; the
+// GEMM epilogue multiplies by 2^e_p. Padding slots get zeros and e_p = 0.
+__global__ void __launch_bounds__(128) gather_f16_kernel(const uint4 *__restrict__ x, int R, int k, int H8,
+                                                         const int32_t *__restrict__ sorted,
+                                                         const int32_t *__restrict__ used_end,
+                                                         uint4 *__restrict__ x16, int32_t *__restrict__ xexp) {
+  __shared__ float wmax[4];
+  pdl_wait();
+  pdl_trigger();
+  const int p = blockIdx.x;
+  if (p >= *used_end) return;
+  const int s = sorted[p];
+  uint4 *dst = x16 + (size_t)p * H8;
+  if (!(s >= 0 && s < R)) {
+    for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) xexp[p] = 0;
+    return;
+  }
+  const uint4 *src = x + (size_t)(s / k) * H8;
+  float m = 0.f;
+  for (int v = threadIdx.x; v < H8; v += blockDim.x) {
+    const uint4 q = src[v];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  // m < 2^(ex) with ex from the fp32 exponent field; e = ex - 15 when positive
+  int e = 0;
+  if (m > 32768.f) {
+    const int ex = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 126;  // m < 2^ex
+    e = min(ex - 15, 254);
+  }
+  const float sc = __uint_as_float((uint32_t)(127 - min(e, 126)) << 23);  // 2^-e (e <= 126)
+  for (int v = threadIdx.x; v < H8; v += blockDim.x) {
+    const uint4 q = src[v];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * sc, __uint_as_float(w[i] & 0xFFFF0000u) * sc);
+      o[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) xexp[p] = min(e, 126);
+}
+
 }  // namespace
+
+moe_status_t launch_gather_f16(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
+                               const int32_t *offsets_end, uint16_t *x16, int32_t *xexp, cudaStream_t stream,
+                               int *launches) {
+  if (P_max == 0) return MOE_OK;
+  const cudaError_t err = launch_pdl(gather_f16_kernel, dim3(P_max), dim3(128), 0, stream,
+                                     reinterpret_cast<const uint4 *>(x), T * k, k, H / 8, sorted_ids, offsets_end,
+                                     reinterpret_cast<uint4 *>(x16), xexp);
+  if (launches) ++*launches;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, int P_max,
                           int32_t *sorted_ids, int32_t *offsets, int32_t *block_ids, int32_t *row_pos,

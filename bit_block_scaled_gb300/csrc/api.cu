@@ -35,7 +35,7 @@ moe_status_t check_weight(const moe_qweight_t *w, int E, int N, int K) {
 }
 
 struct Carve {
-  size_t status, ids, tw, sorted, offsets, blocks, rowpos, xperm, a, xin, lin, outb, total;
+  size_t status, ids, tw, sorted, offsets, blocks, rowpos, xexp, xperm, a, xin, lin, outb, total;
 };
 
 Carve carve(int T, int E, int k, int H, int I, int bm) {
@@ -50,6 +50,7 @@ Carve carve(int T, int E, int k, int H, int I, int bm) {
   c.offsets = o; o += up256((size_t)(E + 1) * 4);
   c.blocks = o; o += up256((size_t)(P / bm) * 4);
   c.rowpos = o; o += up256(R * 4);
+  c.xexp = o; o += up256((size_t)P * 4);       // f16 operand path: per-slot exponents
   c.xperm = o; o += up256((size_t)P * H * 2);  // x_perm, later reused for y
   c.a = o; o += up256((size_t)P * I * 2);
   c.xin = o; o += up256((size_t)T * H * 2);    // staging for moe_forward_host
@@ -167,10 +168,13 @@ moe_status_t moe_unpermute_reduce(const uint16_t *y, const int32_t *row_pos, int
                           &g_last_launches);
 }
 
+// ev (optional): 7 events recorded before the first kernel and after each of
+// the six (route, align, gather, GEMM1, GEMM2, unpermute)
 static moe_status_t forward_impl(const uint16_t *x, const float *logits, const float *sel_bias, int T, int E,
                                  int k, int H, int I, int route, const moe_qweight_t *w13,
                                  const moe_qweight_t *w2, int layout, moe_act_t act, int mul, int bm,
-                                 uint16_t *out, void *ws, cudaStream_t st) {
+                                 uint16_t *out, void *ws, cudaStream_t st, cudaEvent_t *ev = nullptr) {
+  auto mark = [&](int i) { return !ev || cudaEventRecord(ev[i], st) == cudaSuccess; };
   const Carve c = carve(T, E, k, H, I, bm);
   const int P = (int)moe_padded_rows(T, k, E, bm);
   const int R = T * k;
@@ -184,20 +188,35 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
   uint16_t *xperm = at<uint16_t>(ws, c.xperm);
   uint16_t *abuf = at<uint16_t>(ws, c.a);
   uint16_t *ybuf = xperm;  // x_perm is dead once GEMM1 has run
+  int32_t *xexp = at<int32_t>(ws, c.xexp);
   int *n = &g_last_launches;
   moe_status_t s;
+  // NVFP4 swigluoai layers feed the tensor cores f16 operands: E2M1 x E4M3
+  // weights are exact in f16 and expand with the hardware conversion; token
+  // rows are scaled by a power of two into f16 range (undone in the GEMM1
+  // epilogue) and a (rounded to bf16, R1) is held as f16, which is exact
+  const int f16 = (w13->fmt == MOE_FMT_NVFP4 && w2->fmt == MOE_FMT_NVFP4 && act.kind == MOE_ACT_SWIGLUOAI) ? 1 : 0;
+  if (!mark(0)) return MOE_ERR_CUDA;
   if ((s = launch_route(logits, sel_bias, T, E, k, route, ids, tw, status, st, n)) != MOE_OK) return s;
+  if (!mark(1)) return MOE_ERR_CUDA;
   if ((s = launch_align(ids, T, k, E, bm, P, sorted, offs, blocks, rowpos, status, st, n)) != MOE_OK) return s;
-  if ((s = launch_gather(x, T, k, H, P, sorted, offs + E, xperm, st, n)) != MOE_OK) return s;
+  if (!mark(2)) return MOE_ERR_CUDA;
+  s = f16 ? launch_gather_f16(x, T, k, H, P, sorted, offs + E, xperm, xexp, st, n)
+          : launch_gather(x, T, k, H, P, sorted, offs + E, xperm, st, n);
+  if (s != MOE_OK) return s;
+  if (!mark(3)) return MOE_ERR_CUDA;
   const int epi1 = act.kind == MOE_ACT_SWIGLUOAI ? 0 : 1;
   if ((s = launch_grouped_gemm(epi1, *w13, xperm, P, sorted, offs, R, nullptr, 0, layout, act, abuf, I, status, st,
-                               n)) != MOE_OK)
+                               n, f16, xexp)) != MOE_OK)
     return s;
+  if (!mark(4)) return MOE_ERR_CUDA;
   moe_act_t none = {0, 0.f, 0.f};
   if ((s = launch_grouped_gemm(2, *w2, abuf, P, sorted, offs, R, tw, mul ? 1 : 0, 0, none, ybuf, H, status, st,
-                               n)) != MOE_OK)
+                               n, f16)) != MOE_OK)
     return s;
-  return launch_unpermute(ybuf, rowpos, T, k, H, P, out, status, st, n);
+  if (!mark(5)) return MOE_ERR_CUDA;
+  if ((s = launch_unpermute(ybuf, rowpos, T, k, H, P, out, status, st, n)) != MOE_OK) return s;
+  return mark(6) ? MOE_OK : MOE_ERR_CUDA;
 }
 
 static moe_status_t check_forward(const float *sel_bias, int T, int E, int k, int H, int I, int route,
@@ -230,6 +249,35 @@ moe_status_t moe_forward(const uint16_t *x, const float *logits, const float *se
   if (!aligned16(x) || !aligned16(logits) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   return forward_impl(x, logits, sel_bias, T, E, k, H, I, route, w13, w2, gate_up_layout, act, mul_topk_weights,
                       block_m, out, ws, (cudaStream_t)stream);
+}
+
+moe_status_t moe_forward_profile(const uint16_t *x, const float *logits, const float *sel_bias, int T, int E,
+                                 int k, int H, int I, int route, const moe_qweight_t *w13, const moe_qweight_t *w2,
+                                 int gate_up_layout, moe_act_t act, int mul_topk_weights, int block_m, uint16_t *out,
+                                 void *ws, size_t ws_bytes, moe_stream_t stream, float *kernel_ms) {
+  g_last_launches = 0;
+  if (!kernel_ms) return MOE_ERR_INVALID_ARG;
+  moe_status_t s = check_forward(sel_bias, T, E, k, H, I, route, w13, w2, gate_up_layout, act, &block_m, ws,
+                                 ws_bytes);
+  if (s != MOE_OK) return s;
+  for (int i = 0; i < 6; ++i) kernel_ms[i] = 0.f;
+  if (T == 0) return MOE_OK;
+  if (!aligned16(x) || !aligned16(logits) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  cudaEvent_t ev[7];
+  int made = 0;
+  for (; made < 7; ++made)
+    if (cudaEventCreate(&ev[made]) != cudaSuccess) break;
+  if (made == 7) {
+    s = forward_impl(x, logits, sel_bias, T, E, k, H, I, route, w13, w2, gate_up_layout, act, mul_topk_weights,
+                     block_m, out, ws, (cudaStream_t)stream, ev);
+    if (s == MOE_OK && cudaEventSynchronize(ev[6]) != cudaSuccess) s = MOE_ERR_CUDA;
+    for (int i = 0; s == MOE_OK && i < 6; ++i)
+      if (cudaEventElapsedTime(&kernel_ms[i], ev[i], ev[i + 1]) != cudaSuccess) s = MOE_ERR_CUDA;
+  } else {
+    s = MOE_ERR_CUDA;
+  }
+  for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
+  return s;
 }
 
 moe_status_t moe_forward_host(const uint16_t *x_host, const float *logits_host, const float *sel_bias, int T,

@@ -55,4 +55,51 @@ __device__ __forceinline__ uint32_t e8m0_times_2p126_x2(uint32_t e8) {
   return h | (h << 16);
 }
 
+// f16 operand path: f16x2 (both halves) of an E4M3 scale byte (exact; NaN for
+// 0x7F / 0xFF).
+__device__ __forceinline__ uint32_t e4m3_f16x2(uint32_t b) {
+  const uint32_t mag = b & 0x7Fu;
+  __half h;
+  if (mag == 0x7Fu) {
+    h = __ushort_as_half((unsigned short)0x7E00u);
+  } else {
+    float f = __uint_as_float(mag << 20) * 0x1p120f;  // the E4M3 value
+    if (b & 0x80u) f = -f;
+    h = __float2half_rn(f);
+  }
+  const uint32_t u = __half_as_ushort(h);
+  return u | (u << 16);
+}
+
+// f16x2 of the two E2M1 codes in byte `byte` of w (low nibble -> low half).
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t w, int byte) {
+  uint32_t d;
+  switch (byte) {
+    case 0:
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+          : "=r"(d) : "r"(w));
+      break;
+    case 1:
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b1;\n\t}"
+          : "=r"(d) : "r"(w));
+      break;
+    case 2:
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b2;\n\t}"
+          : "=r"(d) : "r"(w));
+      break;
+    default:
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b3;\n\t}"
+          : "=r"(d) : "r"(w));
+      break;
+  }
+  return d;
+}
+
+// a * b on f16 pairs (exact for E2M1 x E4M3 products).
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 }  // namespace moe4

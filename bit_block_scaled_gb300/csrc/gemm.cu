@@ -74,7 +74,7 @@ constexpr int kBarDq0 = 1, kBarEpi = 2, kBarDq1 = 3;
 enum { EPI_SWIGLU = 0, EPI_RELU2 = 1, EPI_WEIGHTED = 2 };
 
 struct Smem {
-  uint32_t x, w, sc, z, lut, offs, ids, tw, bar, misc, total;
+  uint32_t x, w, sc, z, lut, offs, ids, tw, ex, bar, misc, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -94,6 +94,7 @@ __host__ __device__ inline Smem smem_layout(int tile_n, int stages, int kpb, int
   o = align_up(o, 16);
   s.ids = o;  o += kEpiWarps * tile_n * 4;  // one copy per epilogue warp
   s.tw = o;   o += kEpiWarps * tile_n * 4;
+  s.ex = o;   o += kEpiWarps * tile_n * 4;
   o = align_up(o, 8);
   s.bar = o;  o += (2 * kMaxStagesL + 2 * kMaxNA + 8) * 8;
   s.misc = o; o += 64;
@@ -168,7 +169,7 @@ __device__ __forceinline__ TokenTile find_token_tile(const int *offs, int E, int
 
 }  // namespace
 
-template <int FMT, int EPI, int KPB>
+template <int FMT, int EPI, int KPB, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned start (pointer arithmetic on the shared array keeps the
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
   // ------------------------------------------------------------------ setup
   if (tid < 256) {
-    if (FMT == MOE_FMT_NVFP4) lut[tid] = e4m3_times_2p118_x2((uint32_t)tid);
+    if (FMT == MOE_FMT_NVFP4) lut[tid] = F16 ? e4m3_f16x2((uint32_t)tid) : e4m3_times_2p118_x2((uint32_t)tid);
     if (FMT == MOE_FMT_MXFP4) lut[tid] = e8m0_times_2p126_x2((uint32_t)tid);
   }
   if (tid == 32) {
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntiles) {
       const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
       const int n16 = (tt.nrows + 15) & ~15;
-      const uint32_t idesc = idesc_bf16(kTileM, n16);
+      const uint32_t idesc = F16 ? idesc_f16(kTileM, n16) : idesc_bf16(kTileM, n16);
       const uint32_t acc = tmem + acc_stride * rc.slot;
       // the epilogue must have drained this accumulator
       ok = ntiles < nacc || mbar_wait(accempty_bar(rc.slot), rc.phase ^ 1);
@@ -460,7 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
               const uint4 c = *reinterpret_cast<const uint4 *>(w_row + cs.slot * (kTileM * rb) +
                                                               ((ch ^ sw) << 4));
               const uint32_t xw[4] = {c.x, c.y, c.z, c.w};
-              if (FMT == MOE_FMT_NVFP4) {
+              if (FMT == MOE_FMT_NVFP4 && F16) {
+                // hardware E2M1 -> f16 pairs (natural K order), times the f16 scale
+                const uint32_t sb = *reinterpret_cast<const uint16_t *>(sc_row + kb * 4 + hk * 2);
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                  const uint32_t s2 = lut[(sb >> (8 * g)) & 0xFFu];
+#pragma unroll
+                  for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) out[(2 * g + h) * 4 + b] = hmul2(e2m1x2_f16x2(xw[2 * g + h], b), s2);
+                }
+              } else if (FMT == MOE_FMT_NVFP4) {
                 const uint32_t sb = *reinterpret_cast<const uint16_t *>(sc_row + kb * 4 + hk * 2);
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
@@ -533,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
     int *ids_w = ids_s + (warp - kFirstEpiWarp) * p.tile_n;  // this warp's copy of the row ids
     float *tw_w = tw_s + (warp - kFirstEpiWarp) * p.tile_n;
+    int *ex_w = reinterpret_cast<int *>(base + L.ex) + (warp - kFirstEpiWarp) * p.tile_n;
     Ring rc;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -549,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         float w = 0.f;
         if (EPI == EPI_WEIGHTED && p.mul && sid >= 0 && sid < p.num_rows) w = p.topk_w[sid];
         tw_w[i] = w;
+        if (F16 && EPI != EPI_WEIGHTED) ex_w[i] = (i < nrows) ? p.xexp[row0 + i] : 0;
       }
       __syncwarp();
       int n_w, col;
@@ -566,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       // layout GEMM2 reads its activations in): column c sits at 2*(c%4)+c/4
       const int col_st = (col & ~7) | ((col & 3) << 1) | ((col >> 2) & 1);
       float gmul = 1.f;
-      if (FMT == MOE_FMT_NVFP4) gmul = p.gscale[e] * 256.f;  // undo the 2^-8 operand fold
+      if (FMT == MOE_FMT_NVFP4) gmul = F16 ? p.gscale[e] : p.gscale[e] * 256.f;  // bf16: undo the 2^-8 fold
       float bias = 0.f;
       if (p.bias && col_ok) bias = bf16_bits_to_float(p.bias[(size_t)e * p.N + n_w]);
       bool lok = true;
@@ -587,7 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const int tok = c0 + j;
           const int sid = ids_w[tok];
           const bool store = tok < nrows && sid >= 0 && sid < p.num_rows && col_ok;
-          float h = __fadd_rn(__fmul_rn(__uint_as_float(v[j]), gmul), bias);
+          float acc = __uint_as_float(v[j]);
+          if (F16 && EPI != EPI_WEIGHTED)  // undo the activation row's 2^-e (exact)
+            acc = __fmul_rn(acc, __uint_as_float((uint32_t)(127 + ex_w[tok]) << 23));
+          float h = __fadd_rn(__fmul_rn(acc, gmul), bias);
           uint16_t *orow = p.out + (size_t)(row0 + tok) * p.ldo;
           if (EPI == EPI_SWIGLU) {
             const float other = __shfl_xor_sync(0xffffffffu, h, 1);
@@ -595,7 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
               const float g = fminf(h, p.limit);
               const float u = fminf(fmaxf(other, -p.limit), p.limit);
               const float sg = __fdividef(1.0f, 1.0f + __expf(-p.alpha * g));  // fast-math sigmoid
-              orow[col_st] = float_to_bf16_bits((u + 1.0f) * g * sg);
+              const uint16_t ab = float_to_bf16_bits((u + 1.0f) * g * sg);  // R1
+              if (F16)  // the bf16 value, held as f16 for GEMM2, natural column order
+                orow[col] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(ab)));
+              else
+                orow[col_st] = ab;
             }
           } else if (EPI == EPI_RELU2) {
             if (store) {
@@ -654,9 +675,9 @@ int sm_count() {
   return n;
 }
 
-template <int FMT, int EPI, int KPB>
+template <int FMT, int EPI, int KPB, bool F16>
 moe_status_t launch_t(const GemmArgs &a, dim3 grid, uint32_t smem, cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<FMT, EPI, KPB>;
+  auto kern = grouped_gemm_kernel<FMT, EPI, KPB, F16>;
   static uint32_t configured = 0;  // per instantiation; grows monotonically
   if (smem > configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -688,9 +709,11 @@ int choose_tile_n(int num_rows, int E) {
 moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t *x, int P_max,
                                  const int32_t *sorted_ids, const int32_t *expert_offsets, int num_rows,
                                  const float *topk_w, int mul, int layout, moe_act_t act, uint16_t *out,
-                                 int ldo, unsigned int *status, cudaStream_t stream, int *launches) {
+                                 int ldo, unsigned int *status, cudaStream_t stream, int *launches, int f16,
+                                 const int32_t *xexp) {
   if (P_max <= 0 || num_rows <= 0) return MOE_OK;
   if (w.E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if (f16 && (w.fmt != MOE_FMT_NVFP4 || epi == 1 || (epi == 0 && !xexp))) return MOE_ERR_UNSUPPORTED;
   auto enc = encode_fn();
   if (!enc) return MOE_ERR_CUDA;
   GemmArgs a;
@@ -719,7 +742,8 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)a.tile_n};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&a.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box, es,
+    if (enc(&a.tm_x, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<uint16_t *>(x), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MOE_ERR_CUDA;
@@ -731,6 +755,7 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   a.expert_offsets = expert_offsets;
   a.sorted_ids = sorted_ids;
   a.topk_w = topk_w;
+  a.xexp = xexp;
   a.out = out;
   a.status = status;
   a.E = E;
@@ -770,11 +795,17 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   dim3 grid(ctas);
   if (launches) ++*launches;
   const int f = w.fmt;
-#define MOE4_DISPATCH_K(F, K)                                                  \
-  if (f == F && kpb == K) {                                                    \
-    if (epi == 0) return launch_t<F, EPI_SWIGLU, K>(a, grid, smem, stream);    \
-    if (epi == 1) return launch_t<F, EPI_RELU2, K>(a, grid, smem, stream);     \
-    return launch_t<F, EPI_WEIGHTED, K>(a, grid, smem, stream);                \
+  if (f16) {  // NVFP4 only (checked above)
+    if (kpb == 2) return epi == 0 ? launch_t<MOE_FMT_NVFP4, EPI_SWIGLU, 2, true>(a, grid, smem, stream)
+                                  : launch_t<MOE_FMT_NVFP4, EPI_WEIGHTED, 2, true>(a, grid, smem, stream);
+    return epi == 0 ? launch_t<MOE_FMT_NVFP4, EPI_SWIGLU, 4, true>(a, grid, smem, stream)
+                    : launch_t<MOE_FMT_NVFP4, EPI_WEIGHTED, 4, true>(a, grid, smem, stream);
+  }
+#define MOE4_DISPATCH_K(F, K)                                                         \
+  if (f == F && kpb == K) {                                                           \
+    if (epi == 0) return launch_t<F, EPI_SWIGLU, K, false>(a, grid, smem, stream);    \
+    if (epi == 1) return launch_t<F, EPI_RELU2, K, false>(a, grid, smem, stream);     \
+    return launch_t<F, EPI_WEIGHTED, K, false>(a, grid, smem, stream);                \
   }
 #define MOE4_DISPATCH(F) MOE4_DISPATCH_K(F, 2) MOE4_DISPATCH_K(F, 4)
   MOE4_DISPATCH(MOE_FMT_NVFP4)

@@ -19,6 +19,7 @@ struct GemmArgs {
   const int32_t *expert_offsets;
   const int32_t *sorted_ids;
   const float *topk_w;
+  const int32_t *xexp;  // f16 operand path: per-slot exponent of the activation rows (GEMM1)
   uint16_t *out;
   unsigned int *status;
   int E, N, K, P_max, num_rows, ldo, layout, I, mul;
@@ -29,11 +30,15 @@ struct GemmArgs {
 int choose_tile_n(int num_rows, int E);
 int choose_kpb(int tile_n);
 
-// epi: 0 = GEMM1 + swigluoai, 1 = GEMM1 + ReLU^2, 2 = GEMM2 + routing weight
+// epi: 0 = GEMM1 + swigluoai, 1 = GEMM1 + ReLU^2, 2 = GEMM2 + routing weight.
+// f16 = 1 selects the f16 operand path (NVFP4 weights, epi 0 or 2 only): the
+// activations x are f16 in natural column order (GEMM1: rows scaled by
+// 2^-xexp[slot]), and GEMM1 writes a as f16 in natural column order.
 moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t *x, int P_max,
                                  const int32_t *sorted_ids, const int32_t *expert_offsets, int num_rows,
                                  const float *topk_w, int mul, int layout, moe_act_t act, uint16_t *out,
-                                 int ldo, unsigned int *status, cudaStream_t stream, int *launches);
+                                 int ldo, unsigned int *status, cudaStream_t stream, int *launches, int f16 = 0,
+                                 const int32_t *xexp = nullptr);
 
 moe_status_t launch_route(const float *logits, const float *sel_bias, int T, int E, int k, int route,
                           int32_t *ids, float *weights, unsigned int *status, cudaStream_t stream,
@@ -42,6 +47,10 @@ moe_status_t launch_route(const float *logits, const float *sel_bias, int T, int
 moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, int P_max,
                           int32_t *sorted_ids, int32_t *offsets, int32_t *block_ids, int32_t *row_pos,
                           unsigned int *status, cudaStream_t stream, int *launches);
+
+moe_status_t launch_gather_f16(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
+                               const int32_t *offsets_end, uint16_t *x16, int32_t *xexp, cudaStream_t stream,
+                               int *launches);
 
 moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
                            const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches);

@@ -223,6 +223,19 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *logits_host,
                               uint16_t *out_host, void *ws, size_t ws_bytes,
                               moe_stream_t stream);
 
+/* moe_forward, then the device time of each of its six kernels: kernel_ms
+ * (host, 6 floats) receives route, align, gather, GEMM1, GEMM2 and unpermute
+ * in milliseconds, from CUDA events recorded on `stream` around each launch.
+ * Synchronises the stream. For measurement; there is no counterpart on the
+ * source pages. */
+moe_status_t moe_forward_profile(const uint16_t *x, const float *logits,
+                                 const float *sel_bias, int T, int E, int k,
+                                 int H, int I, int route, const moe_qweight_t *w13,
+                                 const moe_qweight_t *w2, int gate_up_layout,
+                                 moe_act_t act, int mul_topk_weights, int block_m,
+                                 uint16_t *out, void *ws, size_t ws_bytes,
+                                 moe_stream_t stream, float *kernel_ms);
+
 /* The same layer with no workspace argument, for callers that cannot
  * allocate device memory (no cudaMalloc where they run: inside a graph
  * capture that forbids allocation, a plugin handed only its input and output

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import (OR, assert_close, built, get_config, gpu_forward, gpu_steps, interleave8,
+from gpu_helpers import (OR, act_of, assert_close, built, get_config, gpu_forward, gpu_steps, interleave8,
                          make, near_tie_ok, oracle_full, ws_status)
 
 pytestmark = pytest.mark.gpu
@@ -316,3 +316,42 @@ SMALL = [
 @pytest.mark.parametrize("fmt,act,H,I,E,T,k,layout", SMALL)
 def test_small_batch_many_experts(fmt, act, H, I, E, T, k, layout):
     test_formats_and_activations(fmt, act, H, I, E, T, k, layout)
+
+
+def test_fused_f16_operands_large_activation_rows():
+    """moe_forward feeds NVFP4 swigluoai layers to the tensor cores as f16
+    operands, each token row scaled by a power of two into f16 range. Rows far
+    outside f16 range (|x| up to 1e9) must still match the oracle."""
+    cfg = get_config("c0", name="bigx", T=24, E=8, k=2, H=256, I=256)
+    L, N = make(cfg, seed=12)
+    scale = torch.ones(cfg.T, 1, device="cuda")
+    scale[3] = 1e9
+    scale[7] = 7e4
+    scale[11] = 3e-3
+    L = dict(L)
+    L["x"] = (L["x"].float() * scale).to(torch.bfloat16)
+    N = dict(N)
+    N["x"] = L["x"].float().cpu().numpy()
+    out, ws = gpu_forward(L, cfg)
+    import bit_block_scaled_gb300 as moe
+    assert moe.moe_read_status(ws) == 0
+    o = oracle_full(N, cfg)
+    assert_close(out.float().cpu().numpy(), o["out"], "out with large rows")
+
+
+def test_forward_profile_matches_forward():
+    """moe_forward_profile runs the same kernels as moe_forward (same output
+    bytes) and reports a positive device time for each of the six."""
+    import bit_block_scaled_gb300 as moe
+    cfg = get_config("c0")
+    L, N = make(cfg)
+    ref, _ = gpu_forward(L, cfg)
+    ws = torch.zeros(moe.moe_workspace_size(cfg.T, cfg.E, cfg.k, cfg.H, cfg.I, 16), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    ms = moe.moe_forward_profile(L["x"], L["logits"], L["sel_bias"], cfg.k, moe.ROUTE[cfg.route], L["w13"],
+                                 L["w2"], 0, act_of(cfg), True, 16, out, ws)
+    assert set(ms) == {"route", "align", "gather", "gemm1", "gemm2", "unpermute"}
+    assert all(v > 0 for v in ms.values())
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert moe.moe_read_status(ws) == 0
