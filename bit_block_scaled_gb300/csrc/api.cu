@@ -191,28 +191,31 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
   int32_t *xexp = at<int32_t>(ws, c.xexp);
   int *n = &g_last_launches;
   moe_status_t s;
-  // NVFP4 swigluoai layers feed the tensor cores f16 operands: E2M1 x E4M3
-  // weights are exact in f16 and expand with the hardware conversion; token
-  // rows are scaled by a power of two into f16 range (undone in the GEMM1
-  // epilogue) and a (rounded to bf16, R1) is held as f16, which is exact
-  const int f16 = (w13->fmt == MOE_FMT_NVFP4 && w2->fmt == MOE_FMT_NVFP4 && act.kind == MOE_ACT_SWIGLUOAI) ? 1 : 0;
+  // NVFP4 layers feed the tensor cores f16 operands: E2M1 x E4M3 weights are
+  // exact in f16 and expand with the hardware conversion; token rows are
+  // scaled by a power of two into f16 range (undone in the GEMM1 epilogue);
+  // with swigluoai, a (rounded to bf16, R1) is held as f16, which is exact.
+  // ReLU^2 layers take f16 operands in GEMM1 only (its output is
+  // not bounded, so a stays bf16)
+  const int f16_1 = w13->fmt == MOE_FMT_NVFP4 ? 1 : 0;
+  const int f16_2 = (f16_1 && w2->fmt == MOE_FMT_NVFP4 && act.kind == MOE_ACT_SWIGLUOAI) ? 1 : 0;
   if (!mark(0)) return MOE_ERR_CUDA;
   if ((s = launch_route(logits, sel_bias, T, E, k, route, ids, tw, status, st, n)) != MOE_OK) return s;
   if (!mark(1)) return MOE_ERR_CUDA;
   if ((s = launch_align(ids, T, k, E, bm, P, sorted, offs, blocks, rowpos, status, st, n)) != MOE_OK) return s;
   if (!mark(2)) return MOE_ERR_CUDA;
-  s = f16 ? launch_gather_f16(x, T, k, H, P, sorted, offs + E, xperm, xexp, st, n)
+  s = f16_1 ? launch_gather_f16(x, T, k, H, P, sorted, offs + E, xperm, xexp, st, n)
           : launch_gather(x, T, k, H, P, sorted, offs + E, xperm, st, n);
   if (s != MOE_OK) return s;
   if (!mark(3)) return MOE_ERR_CUDA;
   const int epi1 = act.kind == MOE_ACT_SWIGLUOAI ? 0 : 1;
   if ((s = launch_grouped_gemm(epi1, *w13, xperm, P, sorted, offs, R, nullptr, 0, layout, act, abuf, I, status, st,
-                               n, f16, xexp)) != MOE_OK)
+                               n, f16_1, xexp)) != MOE_OK)
     return s;
   if (!mark(4)) return MOE_ERR_CUDA;
   moe_act_t none = {0, 0.f, 0.f};
   if ((s = launch_grouped_gemm(2, *w2, abuf, P, sorted, offs, R, tw, mul ? 1 : 0, 0, none, ybuf, H, status, st,
-                               n, f16)) != MOE_OK)
+                               n, f16_2)) != MOE_OK)
     return s;
   if (!mark(5)) return MOE_ERR_CUDA;
   if ((s = launch_unpermute(ybuf, rowpos, T, k, H, P, out, status, st, n)) != MOE_OK) return s;

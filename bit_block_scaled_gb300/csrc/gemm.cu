@@ -713,7 +713,7 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
                                  const int32_t *xexp) {
   if (P_max <= 0 || num_rows <= 0) return MOE_OK;
   if (w.E > kMaxE) return MOE_ERR_UNSUPPORTED;
-  if (f16 && (w.fmt != MOE_FMT_NVFP4 || epi == 1 || (epi == 0 && !xexp))) return MOE_ERR_UNSUPPORTED;
+  if (f16 && (w.fmt != MOE_FMT_NVFP4 || (epi != 2 && !xexp))) return MOE_ERR_UNSUPPORTED;
   auto enc = encode_fn();
   if (!enc) return MOE_ERR_CUDA;
   GemmArgs a;
@@ -796,10 +796,15 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   if (launches) ++*launches;
   const int f = w.fmt;
   if (f16) {  // NVFP4 only (checked above)
-    if (kpb == 2) return epi == 0 ? launch_t<MOE_FMT_NVFP4, EPI_SWIGLU, 2, true>(a, grid, smem, stream)
-                                  : launch_t<MOE_FMT_NVFP4, EPI_WEIGHTED, 2, true>(a, grid, smem, stream);
-    return epi == 0 ? launch_t<MOE_FMT_NVFP4, EPI_SWIGLU, 4, true>(a, grid, smem, stream)
-                    : launch_t<MOE_FMT_NVFP4, EPI_WEIGHTED, 4, true>(a, grid, smem, stream);
+#define MOE4_F16_K(K)                                                                       \
+  if (kpb == K) {                                                                           \
+    if (epi == 0) return launch_t<MOE_FMT_NVFP4, EPI_SWIGLU, K, true>(a, grid, smem, stream); \
+    if (epi == 1) return launch_t<MOE_FMT_NVFP4, EPI_RELU2, K, true>(a, grid, smem, stream);  \
+    return launch_t<MOE_FMT_NVFP4, EPI_WEIGHTED, K, true>(a, grid, smem, stream);           \
+  }
+    MOE4_F16_K(2)
+    MOE4_F16_K(4)
+#undef MOE4_F16_K
   }
 #define MOE4_DISPATCH_K(F, K)                                                         \
   if (f == F && kpb == K) {                                                           \

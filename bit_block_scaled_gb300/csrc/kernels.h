@@ -31,9 +31,10 @@ int choose_tile_n(int num_rows, int E);
 int choose_kpb(int tile_n);
 
 // epi: 0 = GEMM1 + swigluoai, 1 = GEMM1 + ReLU^2, 2 = GEMM2 + routing weight.
-// f16 = 1 selects the f16 operand path (NVFP4 weights, epi 0 or 2 only): the
-// activations x are f16 in natural column order (GEMM1: rows scaled by
-// 2^-xexp[slot]), and GEMM1 writes a as f16 in natural column order.
+// f16 = 1 selects the f16 operand path (NVFP4 weights): the activations x are
+// f16 in natural column order (GEMM1: rows scaled by 2^-xexp[slot]); GEMM1
+// with swigluoai writes a as f16 in natural column order, with ReLU^2 as bf16
+// (interleaved, for a bf16 GEMM2: ReLU^2 outputs are not bounded).
 moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t *x, int P_max,
                                  const int32_t *sorted_ids, const int32_t *expert_offsets, int num_rows,
                                  const float *topk_w, int mul, int layout, moe_act_t act, uint16_t *out,

@@ -355,3 +355,18 @@ def test_forward_profile_matches_forward():
     assert all(v > 0 for v in ms.values())
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert moe.moe_read_status(ws) == 0
+
+
+def test_fused_nvfp4_relu2_matches_oracle():
+    """moe_forward on an NVFP4 ReLU^2 layer (f16 operands in GEMM1 only, a
+    kept in bf16) against the oracle, with sigmoid + bias routing."""
+    cfg = get_config("c0", name="relu2_fused", fmt="nvfp4", act="relu2", H=192, I=320, E=6, T=29, k=3,
+                     route="sigmoid_bias", sel_bias_std=0.1, bias=False)
+    L, N = make(cfg, seed=13)
+    g = gpu_steps(L, cfg)
+    out, ws = gpu_forward(L, cfg)
+    import bit_block_scaled_gb300 as moe
+    assert moe.moe_read_status(ws) == 0
+    o = oracle_full(N, cfg, ids=g["topk_ids"].astype(np.int32), tw=g["topk_weights"])
+    assert_close(out.float().cpu().numpy(), o["out"], "fused relu2 out")
+    assert_close(out.float().cpu().numpy(), g["out"], "fused vs steps", atol=1e-3, rtol=1e-3)
