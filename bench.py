@@ -72,6 +72,17 @@ def gemm_source_hash():
     return h.hexdigest()[:16]
 
 
+def operand_dtype(cfg):
+    """The tensor-core operand type each GEMM of the fused forward uses.
+    NVFP4 expands exactly to f16 (E2M1 value times E4M3 scale); its GEMM1 runs
+    on f16 operands, and GEMM2 too when the activation is swigluoai. The other
+    formats dequantise to bf16. Accumulation is fp32 throughout."""
+    if cfg.fmt == "nvfp4":
+        g2 = "f16" if cfg.act == "swigluoai" else "bf16"
+        return f"GEMM1 f16 / GEMM2 {g2} operands (4-bit weights dequantised), fp32 accumulate"
+    return "bf16 operands (4-bit weights dequantised), fp32 accumulate"
+
+
 def read_traffic(kernel_tag):
     """DRAM bytes per launch of the kernel from the committed ncu summary, if
     it was captured for the current kernel source (else None)."""
@@ -343,7 +354,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 operands (4-bit weights dequantised), fp32 accumulate",
+        "dtype": operand_dtype(cfg),
         "data": "synthetic (seeded; weights N(0,0.02) quantised per the workload recipe)",
         "config": {"workload": cfg.workload, "name": args.config, "T": T, "E": E, "top_k": k, "H": H,
                    "I": I, "format": cfg.fmt, "activation": cfg.act, "block_m": bm,
