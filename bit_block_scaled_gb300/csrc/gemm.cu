@@ -182,10 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   constexpr uint32_t rb = 32u * KPB;       // packed bytes per weight row per stage
   const uint32_t bar0 = smem_u32(base + L.bar);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStagesL + s); };
+  // done_bar(slot): the MMAs of the stage in that ring slot have completed, so
+  // both the slot's shared memory and the stage's TMEM operand buffer are free
+  auto done_bar = [&](int s) { return bar0 + 8u * (kMaxStagesL + s); };
   constexpr int kB2 = 2 * kMaxStagesL, kB3 = kB2 + 2 * kMaxNA;
   auto dq_bar = [&](int s) { return bar0 + 8u * (kB2 + s); };
-  auto afree_bar = [&](int s) { return bar0 + 8u * (kB2 + kMaxNA + s); };
   auto scfull_bar = [&](int s) { return bar0 + 8u * (kB3 + s); };
   auto scempty_bar = [&](int s) { return bar0 + 8u * (kB3 + 2 + s); };
   auto accfull_bar = [&](int s) { return bar0 + 8u * (kB3 + 4 + s); };
@@ -206,11 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   if (tid == 32) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(done_bar(s), 1);
     }
     for (int s = 0; s < NA; ++s) {
       mbar_init(dq_bar(s), kDqGroupThreads);
-      mbar_init(afree_bar(s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(scfull_bar(s), 1);
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       }
       rsc.advance(2);
       for (int st = 0; st < NS; ++st) {
-        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(empty_bar(rst.slot), rst.phase ^ 1);
+        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(done_bar(rst.slot), rst.phase ^ 1);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         // one elected lane
         const uint32_t aa = tmem + a_col + (32u * kpb) * ra.slot;
         const uint32_t xb = x_s + rs.slot * kpb * (p.tile_n * 128);
-        const uint32_t fb = afree_bar(ra.slot), eb = empty_bar(rs.slot);
+        const uint32_t db = done_bar(rs.slot);
         if (elect_one()) {
 #pragma unroll
           for (int j = 0; j < kpb; ++j) {
@@ -381,8 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 umma_bf16_ts(acc, aa + 32u * j + 8u * kk, bd + 2u * kk, idesc, (kb0 + j + kk) != 0);
             }
           }
-          umma_commit(fb);
-          umma_commit(eb);
+          umma_commit(db);  // one commit frees the ring slot and the operand buffer
         }
         __syncwarp();
         ra.advance(NA);
@@ -414,7 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // width: 16-byte chunk index ^= address bits [7, 7 + log2(kpb) + 1)
     const int sw = (int)(((uint32_t)pr * rb >> 7) & (uint32_t)(2 * kpb - 1));
     const uint32_t t_a = tmem + ((uint32_t)(q4 * 32) << 16) + a_col;
-    Ring cs, ca, rsc;
+    // cl: ring position of stage kdone - NA, the previous user of this stage's
+    // operand buffer (its done barrier says the buffer is free; NA <= stages,
+    // so that barrier cannot have moved on by a whole lap)
+    Ring cs, ca, rsc, cl;
     int kdone = 0;  // K stages dequantised so far (all tiles)
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -436,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if ((kdone & 1) != grp) {  // the other group's stage
           ca.advance(NA);
           cs.advance(p.stages);
+          if (kdone >= NA) cl.advance(p.stages);
           continue;
         }
         const int kb0 = st * kpb;
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         lok = true;
         if (lead)
           lok = mbar_wait(full_bar(cs.slot), cs.phase) &&
-                (kdone < NA || mbar_wait(afree_bar(ca.slot), ca.phase ^ 1)) && !misc[1];
+                (kdone < NA || mbar_wait(done_bar(cl.slot), cl.phase)) && !misc[1];
         ok = bar_and(gbar, kDqGroupThreads, lok);
         if (!ok) {
           fail(lead && lane == 0);
@@ -531,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         mbar_arrive(dq_bar(ca.slot));
         ca.advance(NA);
         cs.advance(p.stages);
+        if (kdone >= NA) cl.advance(p.stages);
       }
       if (!ok) break;
       mbar_arrive(scempty_bar(rsc.slot));  // done with this tile's scales
@@ -783,6 +787,9 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   int stages = kMaxStagesL;
   while (stages > 2 && smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes).total > budget) --stages;
   a.stages = stages;
+  // an operand buffer is freed by the done barrier of its previous stage's
+  // ring slot, which must not have been reused meanwhile: NA <= stages
+  if (a.na > stages) a.na = stages;
   uint32_t smem = smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes).total;
   // one CTA per SM: it allocates all of TMEM
   if (smem < 120 * 1024) smem = 120 * 1024;
