@@ -183,13 +183,13 @@ __global__ void __launch_bounds__(128) gather_f16_kernel(const uint4 *__restrict
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
   __syncthreads();
   m = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-  // m < 2^(ex) with ex from the fp32 exponent field; e = ex - 15 when positive
-  int e = 0;
-  if (m > 32768.f) {
-    const int ex = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 126;  // m < 2^ex
-    e = min(ex - 15, 254);
-  }
-  const float sc = __uint_as_float((uint32_t)(127 - min(e, 126)) << 23);  // 2^-e (e <= 126)
+  // m < 2^ex with ex from the fp32 exponent field; the row is scaled by 2^-e,
+  // e = ex - 15, so that its largest entry lands in [2^14, 2^15): below the f16
+  // maximum, and every bf16 entry down to 2^-31 of the row's largest stays
+  // exact in f16 (normal down to 2^-28 of it, subnormal with 8 bits below)
+  const int ex = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 126;
+  const int e = max(-126, min(ex - 15, 126));
+  const float sc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
   for (int v = threadIdx.x; v < H8; v += blockDim.x) {
     const uint4 q = src[v];
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};

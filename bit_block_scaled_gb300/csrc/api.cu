@@ -196,9 +196,17 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
   // scaled by a power of two into f16 range (undone in the GEMM1 epilogue);
   // with swigluoai, a (rounded to bf16, R1) is held as f16, which is exact.
   // ReLU^2 layers take f16 operands in GEMM1 only (its output is
-  // not bounded, so a stays bf16)
-  const int f16_1 = w13->fmt == MOE_FMT_NVFP4 ? 1 : 0;
-  const int f16_2 = (f16_1 && w2->fmt == MOE_FMT_NVFP4 && act.kind == MOE_ACT_SWIGLUOAI) ? 1 : 0;
+  // not bounded, so a stays bf16). MXFP4 weights take the same path with their power-of-two scales folded
+  // by 2^12 into f16 range. GEMM2 runs on f16 operands only when a is f16
+  // (GEMM1 on f16 operands with swigluoai) and its own weights are FP4.
+  auto fp4 = [](const moe_qweight_t *w) { return w->fmt == MOE_FMT_NVFP4 || w->fmt == MOE_FMT_MXFP4; };
+  const int f16_1 = fp4(w13) ? 1 : 0;
+  // a is held as f16 times 2^9 (exact for |a| >= 2^-26 once rounded to bf16),
+  // so |a| <= (limit + 1) * max(limit, 0.2785 / alpha) must stay within 64:
+  // the gpt-oss constants (alpha 1.702, limit 7) give 56
+  const bool a_fits = act.alpha > 0.f && act.limit >= 0.f &&
+                      (act.limit + 1.f) * fmaxf(act.limit, 0.2785f / act.alpha) <= 64.f;
+  const int f16_2 = (f16_1 && fp4(w2) && act.kind == MOE_ACT_SWIGLUOAI && a_fits) ? 1 : 0;
   if (!mark(0)) return MOE_ERR_CUDA;
   if ((s = launch_route(logits, sel_bias, T, E, k, route, ids, tw, status, st, n)) != MOE_OK) return s;
   if (!mark(1)) return MOE_ERR_CUDA;
@@ -210,7 +218,7 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
   if (!mark(3)) return MOE_ERR_CUDA;
   const int epi1 = act.kind == MOE_ACT_SWIGLUOAI ? 0 : 1;
   if ((s = launch_grouped_gemm(epi1, *w13, xperm, P, sorted, offs, R, nullptr, 0, layout, act, abuf, I, status, st,
-                               n, f16_1, xexp)) != MOE_OK)
+                               n, f16_1 | (f16_2 << 1), xexp)) != MOE_OK)
     return s;
   if (!mark(4)) return MOE_ERR_CUDA;
   moe_act_t none = {0, 0.f, 0.f};

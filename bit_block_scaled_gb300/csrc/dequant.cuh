@@ -71,6 +71,28 @@ __device__ __forceinline__ uint32_t e4m3_f16x2(uint32_t b) {
   return u | (u << 16);
 }
 
+// f16 operand path for MXFP4: f16x2 (both halves) of 2^(e8 - 115), the E8M0
+// scale 2^(e8 - 127) times 2^12 (the epilogue multiplies by 2^-12). For the
+// exponents the kernels accept (e8 <= 128) every E2M1 value times it stays
+// below 6 * 2^13 < 65504, and is exact down to e8 = 92 (0.5 * 2^-23); e8 = 91
+// is the smallest power of two f16 holds (2^-24), smaller scales give 0.
+// 255 (NaN) gives NaN, exponents above 128 infinity (they are also reported).
+__device__ __forceinline__ uint32_t e8m0_f16x2(uint32_t e8) {
+  uint32_t h;
+  if (e8 == 0xFFu) {
+    h = 0x7E00u;
+  } else if (e8 > 128u) {
+    h = 0x7C00u;
+  } else if (e8 >= 101u) {  // normal: exponent field (e8 - 115) + 15
+    h = (e8 - 100u) << 10;
+  } else if (e8 >= 91u) {  // subnormal: 2^(e8 - 115) = 2^(e8 - 91) * 2^-24
+    h = 1u << (e8 - 91u);
+  } else {
+    h = 0u;
+  }
+  return h | (h << 16);
+}
+
 // f16x2 of the two E2M1 codes in byte `byte` of w (low nibble -> low half).
 __device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t w, int byte) {
   uint32_t d;

@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   // ------------------------------------------------------------------ setup
   if (tid < 256) {
     if (FMT == MOE_FMT_NVFP4) lut[tid] = F16 ? e4m3_f16x2((uint32_t)tid) : e4m3_times_2p118_x2((uint32_t)tid);
-    if (FMT == MOE_FMT_MXFP4) lut[tid] = e8m0_times_2p126_x2((uint32_t)tid);
+    if (FMT == MOE_FMT_MXFP4) lut[tid] = F16 ? e8m0_f16x2((uint32_t)tid) : e8m0_times_2p126_x2((uint32_t)tid);
   }
   if (tid == 32) {
     for (int s = 0; s < p.stages; ++s) {
@@ -492,12 +492,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint32_t e8 = sc_row[kb * 2 + hk];
                 if (e8 > 128u && e8 != 255u) raise_status(p.status, MOE_ERR_SCALE_RANGE);
                 const uint32_t s2 = lut[e8];
+                if (F16) {  // hardware E2M1 -> f16 pairs (natural K order) times 2^(e8 - 115)
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                  uint32_t o4[4];
-                  e2m1x8_raw(xw[h], o4);
+                  for (int h = 0; h < 4; ++h)
 #pragma unroll
-                  for (int q = 0; q < 4; ++q) out[h * 4 + q] = bmul2(o4[q], s2);
+                    for (int b = 0; b < 4; ++b) out[h * 4 + b] = hmul2(e2m1x2_f16x2(xw[h], b), s2);
+                } else {
+#pragma unroll
+                  for (int h = 0; h < 4; ++h) {
+                    uint32_t o4[4];
+                    e2m1x8_raw(xw[h], o4);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) out[h * 4 + q] = bmul2(o4[q], s2);
+                  }
                 }
               } else {  // INT4, one group of 64 per K block
                 // bf16_rne((q - z) * s) with a single rounding, on bf16 pairs:
@@ -584,7 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       // layout GEMM2 reads its activations in): column c sits at 2*(c%4)+c/4
       const int col_st = (col & ~7) | ((col & 3) << 1) | ((col >> 2) & 1);
       float gmul = 1.f;
-      if (FMT == MOE_FMT_NVFP4) gmul = F16 ? p.gscale[e] : p.gscale[e] * 256.f;  // bf16: undo the 2^-8 fold
+      // undo the operands' power-of-two folds: bf16 NVFP4 weights carry 2^-8,
+      // f16 MXFP4 weights 2^12, and a f16 GEMM2 reads a scaled by 2^9
+      const float afold = (F16 && EPI == EPI_WEIGHTED) ? 0x1p-9f : 1.f;
+      if (FMT == MOE_FMT_NVFP4) gmul = F16 ? p.gscale[e] * afold : p.gscale[e] * 256.f;
+      if (FMT == MOE_FMT_MXFP4 && F16) gmul = 0x1p-12f * afold;
       float bias = 0.f;
       if (p.bias && col_ok) bias = bf16_bits_to_float(p.bias[(size_t)e * p.N + n_w]);
       bool lok = true;
@@ -617,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
               const float u = fminf(fmaxf(other, -p.limit), p.limit);
               const float sg = __fdividef(1.0f, 1.0f + __expf(-p.alpha * g));  // fast-math sigmoid
               const uint16_t ab = float_to_bf16_bits((u + 1.0f) * g * sg);  // R1
-              if (F16)  // the bf16 value, held as f16 for GEMM2, natural column order
-                orow[col] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(ab)));
+              if (F16 && p.a_f16)  // the bf16 value times 2^9, held as f16 for an f16 GEMM2, natural order
+                orow[col] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(ab) * 512.f));
               else
                 orow[col_st] = ab;
             }
@@ -717,7 +728,12 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
                                  const int32_t *xexp) {
   if (P_max <= 0 || num_rows <= 0) return MOE_OK;
   if (w.E > kMaxE) return MOE_ERR_UNSUPPORTED;
-  if (f16 && (w.fmt != MOE_FMT_NVFP4 || (epi != 2 && !xexp))) return MOE_ERR_UNSUPPORTED;
+  // f16: bit 0 = f16 operands (NVFP4 / MXFP4 weights), bit 1 = GEMM1 writes a
+  // as f16 in natural column order (for an f16 GEMM2) instead of bf16
+  const int a_f16 = (f16 >> 1) & 1;
+  f16 &= 1;
+  if (f16 && ((w.fmt != MOE_FMT_NVFP4 && w.fmt != MOE_FMT_MXFP4) || (epi != 2 && !xexp)))
+    return MOE_ERR_UNSUPPORTED;
   auto enc = encode_fn();
   if (!enc) return MOE_ERR_CUDA;
   GemmArgs a;
@@ -771,6 +787,7 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   a.layout = layout;
   a.I = (epi == 0) ? N / 2 : N;
   a.mul = mul;
+  a.a_f16 = a_f16;
   a.alpha = act.alpha;
   a.limit = act.limit;
   a.m_tiles = (epi == 0) ? (N / 2 + 63) / 64 : (N + kTileM - 1) / kTileM;
@@ -802,15 +819,17 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   dim3 grid(ctas);
   if (launches) ++*launches;
   const int f = w.fmt;
-  if (f16) {  // NVFP4 only (checked above)
-#define MOE4_F16_K(K)                                                                       \
-  if (kpb == K) {                                                                           \
-    if (epi == 0) return launch_t<MOE_FMT_NVFP4, EPI_SWIGLU, K, true>(a, grid, smem, stream); \
-    if (epi == 1) return launch_t<MOE_FMT_NVFP4, EPI_RELU2, K, true>(a, grid, smem, stream);  \
-    return launch_t<MOE_FMT_NVFP4, EPI_WEIGHTED, K, true>(a, grid, smem, stream);           \
+  if (f16) {  // NVFP4 or MXFP4 (checked above)
+#define MOE4_F16_K(F, K)                                                          \
+  if (f == F && kpb == K) {                                                       \
+    if (epi == 0) return launch_t<F, EPI_SWIGLU, K, true>(a, grid, smem, stream); \
+    if (epi == 1) return launch_t<F, EPI_RELU2, K, true>(a, grid, smem, stream);  \
+    return launch_t<F, EPI_WEIGHTED, K, true>(a, grid, smem, stream);             \
   }
-    MOE4_F16_K(2)
-    MOE4_F16_K(4)
+    MOE4_F16_K(MOE_FMT_NVFP4, 2)
+    MOE4_F16_K(MOE_FMT_NVFP4, 4)
+    MOE4_F16_K(MOE_FMT_MXFP4, 2)
+    MOE4_F16_K(MOE_FMT_MXFP4, 4)
 #undef MOE4_F16_K
   }
 #define MOE4_DISPATCH_K(F, K)                                                         \

@@ -22,7 +22,7 @@ struct GemmArgs {
   const int32_t *xexp;  // f16 operand path: per-slot exponent of the activation rows (GEMM1)
   uint16_t *out;
   unsigned int *status;
-  int E, N, K, P_max, num_rows, ldo, layout, I, mul;
+  int E, N, K, P_max, num_rows, ldo, layout, I, mul, a_f16;
   float alpha, limit;
   int tile_n, stages, kpb, sc_row_bytes, z_row_bytes, m_tiles, nacc, na;
 };
@@ -31,10 +31,13 @@ int choose_tile_n(int num_rows, int E);
 int choose_kpb(int tile_n);
 
 // epi: 0 = GEMM1 + swigluoai, 1 = GEMM1 + ReLU^2, 2 = GEMM2 + routing weight.
-// f16 = 1 selects the f16 operand path (NVFP4 weights): the activations x are
-// f16 in natural column order (GEMM1: rows scaled by 2^-xexp[slot]); GEMM1
-// with swigluoai writes a as f16 in natural column order, with ReLU^2 as bf16
-// (interleaved, for a bf16 GEMM2: ReLU^2 outputs are not bounded).
+// f16 bit 0 selects the f16 operand path (NVFP4 or MXFP4 weights): the
+// activations x are f16 in natural column order (GEMM1: rows scaled by
+// 2^-xexp[slot]). f16 bit 1 (GEMM1 with swigluoai, when GEMM2 also runs on f16
+// operands) writes a times 2^9 as f16 in natural column order (the f16 GEMM2
+// undoes the 2^9 in its epilogue); otherwise GEMM1 writes a
+// as bf16 with interleaved columns, as a bf16 GEMM2 reads it (ReLU^2 outputs
+// are not bounded, so they always stay bf16).
 moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t *x, int P_max,
                                  const int32_t *sorted_ids, const int32_t *expert_offsets, int num_rows,
                                  const float *topk_w, int mul, int layout, moe_act_t act, uint16_t *out,

@@ -370,3 +370,60 @@ def test_fused_nvfp4_relu2_matches_oracle():
     o = oracle_full(N, cfg, ids=g["topk_ids"].astype(np.int32), tw=g["topk_weights"])
     assert_close(out.float().cpu().numpy(), o["out"], "fused relu2 out")
     assert_close(out.float().cpu().numpy(), g["out"], "fused vs steps", atol=1e-3, rtol=1e-3)
+
+
+# w13 and w2 in different formats: GEMM2 runs on f16 operands only when GEMM1
+# wrote a as f16, so every combination must hand a over in the layout the
+# second GEMM reads
+MIXED = [
+    # fmt of w13, fmt of w2, act
+    ("nvfp4", "int4", "swigluoai"),
+    ("nvfp4", "mxfp4", "swigluoai"),
+    ("mxfp4", "nvfp4", "swigluoai"),
+    ("int4", "mxfp4", "swigluoai"),
+    ("mxfp4", "int4", "relu2"),
+]
+
+
+@pytest.mark.parametrize("f13,f2,act", MIXED)
+def test_fused_mixed_weight_formats(f13, f2, act):
+    import bit_block_scaled_gb300 as moe
+    from synth import make_layer, to_numpy
+    base = dict(name=f"mixed_{f13}_{f2}", act=act, H=320, I=256, E=6, T=21, k=2)
+    cfg13 = get_config("c0", fmt=f13, **base)
+    cfg2 = get_config("c0", fmt=f2, **base)
+    L = dict(make_layer(cfg13, 17, device="cuda"))
+    L["w2"] = make_layer(cfg2, 17, device="cuda")["w2"]
+    N = to_numpy(L)
+    g = gpu_steps(L, cfg13)
+    out, ws = gpu_forward(L, cfg13)
+    assert moe.moe_read_status(ws) == 0
+    o = oracle_full(N, cfg13, ids=g["topk_ids"].astype(np.int32), tw=g["topk_weights"])
+    assert_close(out.float().cpu().numpy(), o["out"], f"fused out, w13 {f13}, w2 {f2}")
+    assert_close(g["out"], o["out"], f"steps out, w13 {f13}, w2 {f2}")
+
+
+def test_fused_mxfp4_f16_scale_range():
+    """The fused forward runs MXFP4 layers on f16 operands, each E8M0 scale
+    folded by 2^12 into f16 range: the largest accepted exponent (128, a scale
+    of 2) must not overflow, and exponents down to 92 stay exact; 91 and below
+    lose bits or vanish, which is far inside the tolerance."""
+    import bit_block_scaled_gb300 as moe
+    from synth import make_layer, to_numpy
+    cfg = get_config("c0", name="mx_range", fmt="mxfp4", H=256, I=192, E=4, T=12, k=2)
+    L = dict(make_layer(cfg, 3, device="cuda"))
+    for key in ("w13", "w2"):
+        w = dict(L[key])
+        sc = w["scales"].clone()
+        sc[0, :16, 0] = 128
+        sc[1, :16, 1] = 127
+        sc[1, 16:32, 0] = 92
+        sc[2, :16, 2] = 91
+        sc[3, :16, 1] = 60
+        w["scales"] = sc
+        L[key] = w
+    N = to_numpy(L)
+    out, ws = gpu_forward(L, cfg)
+    assert moe.moe_read_status(ws) == 0
+    o = oracle_full(N, cfg)
+    assert_close(out.float().cpu().numpy(), o["out"], "mxfp4 f16 path, extreme scales")
