@@ -24,7 +24,8 @@ STATUS_BYTES = 256
 EXPORTS = ("moe_padded_rows", "moe_workspace_size", "moe_route_topk", "moe_align_permute",
            "moe_grouped_gemm1_act", "moe_grouped_gemm2_weighted", "moe_unpermute_reduce",
            "moe_forward", "moe_forward_host", "moe_read_status", "moe_clear_status",
-           "moe_status_string", "moe_last_launch_count", "moe_forward_static", "moe_forward_profile")
+           "moe_status_string", "moe_last_launch_count", "moe_forward_static", "moe_forward_profile",
+           "moe_import_gptq_int4", "moe_import_modelopt_global_scale")
 
 
 class MoeError(RuntimeError):
@@ -67,6 +68,8 @@ _SIGS = {
     "moe_clear_status": (_i32, [_vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_i32]),
     "moe_last_launch_count": (_i32, []),
+    "moe_import_gptq_int4": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_import_modelopt_global_scale": (_i32, [ctypes.c_float, _i32, _vp]),
 }
 
 _lib = None
@@ -241,3 +244,42 @@ def moe_status_string(code):
 
 def moe_last_launch_count():
     return int(load().moe_last_launch_count())
+
+
+def _host_ptr(a):
+    """Pointer to a C-contiguous numpy array in host memory (None stays NULL)."""
+    if a is None:
+        return None
+    import numpy as np
+    assert isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"], "host arrays must be C-contiguous numpy"
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def moe_import_gptq_int4(qweight_, qzeros, scales, g_idx=None, group_size=64, zero_offset=0):
+    """GPTQ INT4 tensors of one linear layer (numpy, host) -> (q uint8 [N, K/2],
+    scales fp16 [N, K/64], zeros uint8 [N, ceil(K/128)]) in the library's layout."""
+    import numpy as np
+    qweight_ = np.ascontiguousarray(qweight_, dtype=np.int32)
+    qzeros = np.ascontiguousarray(qzeros, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.float16)
+    if g_idx is not None:
+        g_idx = np.ascontiguousarray(g_idx, dtype=np.int32)
+    K8, N = qweight_.shape
+    K = 8 * K8
+    q = np.empty((N, K // 2), dtype=np.uint8)
+    s_out = np.empty((N, max(K // 64, 1)), dtype=np.float16)
+    z_out = np.empty((N, max((K // 64 + 1) // 2, 1)), dtype=np.uint8)
+    _check(load().moe_import_gptq_int4(_host_ptr(qweight_), _host_ptr(qzeros), _host_ptr(scales),
+                                       _host_ptr(g_idx), K, N, group_size, zero_offset, _host_ptr(q),
+                                       _host_ptr(s_out), _host_ptr(z_out)), "moe_import_gptq_int4")
+    return q, s_out, z_out
+
+
+def moe_import_modelopt_global_scale(weight_scale_2, E):
+    """The per-expert global scales (numpy float32 [E]) for a ModelOpt
+    checkpoint's single weight_scale_2."""
+    import numpy as np
+    g = np.empty(E, dtype=np.float32)
+    _check(load().moe_import_modelopt_global_scale(float(weight_scale_2), E, _host_ptr(g)),
+           "moe_import_modelopt_global_scale")
+    return g

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe4.so")
-SOURCES = ["api.cu", "route.cu", "align.cu", "gemm.cu", "unpermute.cu", "static_ws.cu"]
+SOURCES = ["api.cu", "route.cu", "align.cu", "gemm.cu", "unpermute.cu", "static_ws.cu", "convert.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

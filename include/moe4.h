@@ -274,6 +274,47 @@ const char *moe_status_string(int status);
 /* Number of kernels the last moe_forward call on this thread launched. */
 int moe_last_launch_count(void);
 
+/* ---------------------------------------------------------------------------
+ * Checkpoint-layout import (host memory, host only, no CUDA calls; for load
+ * time). They rewrite the expert weights of the pages' checkpoints into the
+ * moe_qweight_t layout above.
+ * ------------------------------------------------------------------------- */
+
+/* One GPTQ INT4 linear layer (N outputs, K inputs, group 64) of one expert
+ * [GPTQ "1. Quantize": per-expert gate_proj / up_proj / down_proj with
+ * qweight, qzeros, scales, g_idx; MARLIN "Reproducer": qweight is the int32
+ * [K/8][N] view of the [N][K/2] code bytes]. In:
+ *   qweight int32 [K/8][N]: the code of input k = 8i + j of output n in bits
+ *           4j..4j+3 of qweight[i][n]
+ *   qzeros  int32 [K/64][N/8]: the zero point of output n = 8m + j, group g,
+ *           in bits 4j..4j+3 of qzeros[g][m], stored as (zero - zero_offset)
+ *   scales  fp16 [K/64][N]
+ *   g_idx   int32 [K] or NULL: group of input k; must be k / 64
+ * Out (caller-owned): q uint8 [N][K/2] (low nibble = even k), scales_out fp16
+ * [N][K/64], zeros_out uint8 [N][ceil(K/128)] (low nibble = even group), i.e.
+ * rows of moe_qweight_t q / scales / zeros. For W13, convert gate_proj into
+ * rows 0..I-1 and up_proj into rows I..2I-1 (pointers offset by I rows) and
+ * pass MOE_LAYOUT_CONCAT. zero_offset: 0 when qzeros holds the zero points
+ * themselves, 1 when it holds them minus one.
+ * Errors: MOE_ERR_INVALID_ARG (null pointer, K or N not a multiple of 64,
+ * zero_offset not 0 or 1); MOE_ERR_UNSUPPORTED (group_size != 64, a g_idx
+ * other than k / 64, a zero point outside 0..15). Nothing is written on
+ * error. */
+moe_status_t moe_import_gptq_int4(const int32_t *qweight, const int32_t *qzeros,
+                                  const uint16_t *scales, const int32_t *g_idx,
+                                  int K, int N, int group_size, int zero_offset,
+                                  uint8_t *q, uint16_t *scales_out,
+                                  uint8_t *zeros_out);
+
+/* ModelOpt NVFP4 [NVFP4 "Gap 2", 2b]: the codes (two E2M1 per byte, low
+ * nibble = even k) and E4M3 group-16 scales already have the moe_qweight_t
+ * layout, but the checkpoint keeps weight_scale_2 as one scalar where this
+ * library takes one global scale per expert: gscale[e] = weight_scale_2 for
+ * e < E (host array of E floats). MOE_ERR_INVALID_ARG for a null pointer or
+ * E outside 1..256. */
+moe_status_t moe_import_modelopt_global_scale(float weight_scale_2, int E,
+                                              float *gscale);
+
 #ifdef __cplusplus
 }
 #endif
