@@ -24,6 +24,14 @@ path follows as well:
       routing weight is applied in the epilogue; y = bf16(z);
   R3  unpermute: fp32 sum over j = 0..k-1 in that order, rounded to bf16.
 
+Where the routing weight is applied (``mul_topk_weights``): 0 nowhere, 1 (or
+True) in the GEMM2 epilogue as above, 2 on the input. The pages name the switch
+(``apply_router_weight_on_input``; with it off, GEMM2 multiplies -- vLLM issue
+"moe_wna16_marlin_gemm applies wrong per-row topk weights", "Minimal repro")
+but do not spell out the other setting. Its plain reading, taken here: every
+routed row (t, j) enters GEMM1 as  Rin  x_in = bf16(fp32(x[t] * w_tj)), and
+GEMM2 does not multiply.
+
 Formulas that the pages name but do not print, and the readings taken:
   * swigluoai (vLLM issue "gpt-oss-20b NVFP4 inference is broken", Gap 3a/3b:
     ``gemm1_alpha/beta/clamp_limit``): gate = min(gate, limit),
@@ -53,6 +61,13 @@ from . import routing as _routing
 FMT_NVFP4, FMT_MXFP4, FMT_INT4 = 0, 1, 2
 ACT_SWIGLUOAI, ACT_RELU2 = 0, 1
 LAYOUT_INTERLEAVED, LAYOUT_CONCAT = 0, 1
+MUL_NONE, MUL_OUTPUT, MUL_INPUT = 0, 1, 2
+
+
+def weight_rows_on_input(x_rows, row_weights):
+    """Rin: bf16(fp32(x * w)) for each routed row and its own routing weight."""
+    prod = np.asarray(x_rows, np.float64) * np.asarray(row_weights, np.float64)[:, None]
+    return bf16_rne(f32(prod))
 
 
 # --------------------------------------------------------------------------- R0
@@ -240,7 +255,7 @@ def grouped_gemm2_weighted(a, expert_offsets, sorted_token_ids, num_rows, w2,
         if slots.size == 0:
             continue
         W = dequant(w2, e)
-        rw = tw[s[slots]] if mul_topk_weights else None
+        rw = tw[s[slots]] if mul_topk_weights == MUL_OUTPUT else None
         y[slots] = expert_gemm2(a[slots], W, gscale_of(w2, e), bias_of(w2, e), rw)
     return y
 
@@ -262,6 +277,11 @@ def moe_forward(x, logits, w13, w2, k, route_mode=_routing.ROUTE_TOPK_SOFTMAX,
     meta = _align.align_permute(topk_ids, E, block_m)
     R = T * k
     x_perm = _align.gather_rows(x, meta["sorted_token_ids"], k)
+    if mul_topk_weights == MUL_INPUT:
+        srt = np.asarray(meta["sorted_token_ids"])
+        used = np.nonzero(srt < R)[0]
+        x_perm = x_perm.copy()
+        x_perm[used] = weight_rows_on_input(x_perm[used], topk_weights.reshape(-1)[srt[used]])
     a = grouped_gemm1_act(x_perm, meta["expert_offsets"], meta["sorted_token_ids"],
                           R, w13, act, layout, alpha, limit)
     y = grouped_gemm2_weighted(a, meta["expert_offsets"], meta["sorted_token_ids"],
@@ -296,9 +316,12 @@ def moe_forward_tokens(x, topk_ids, topk_weights, w13, w2, tokens, act=ACT_SWIGL
         for j in range(k):
             e = int(ids[t, j])
             W13, W2 = ops(e)
-            a = expert_gemm1_act(x[t:t + 1], W13, gscale_of(w13, e), bias_of(w13, e),
+            xin = x[t:t + 1]
+            if mul_topk_weights == MUL_INPUT:
+                xin = weight_rows_on_input(xin, tw[t, j:j + 1])
+            a = expert_gemm1_act(xin, W13, gscale_of(w13, e), bias_of(w13, e),
                                  act, layout, alpha, limit)
-            rw = tw[t, j:j + 1] if mul_topk_weights else None
+            rw = tw[t, j:j + 1] if mul_topk_weights == MUL_OUTPUT else None
             y = expert_gemm2(a, W2, gscale_of(w2, e), bias_of(w2, e), rw)
             acc = (acc + y[0]).astype(np.float32)
         out[i] = bf16_rne(acc)

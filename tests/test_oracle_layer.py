@@ -65,6 +65,8 @@ def _brute_dequant(w, e):
 
 
 def _brute_layer(Lr, cfg, ids, tw, mul=True):
+    """mul: False/0 no routing weight, True/1 on the output (GEMM2 epilogue),
+    2 on the input (each routed row bf16(fp32(x * w)) before GEMM1)."""
     x = Lr["x"]
     w13, w2 = Lr["w13"], Lr["w2"]
     T, k = ids.shape
@@ -78,9 +80,12 @@ def _brute_layer(Lr, cfg, ids, tw, mul=True):
             if e not in cache:
                 cache[e] = (_brute_dequant(w13, e), _brute_dequant(w2, e))
             W13, W2 = cache[e]
+            xr = [float(x[t, i]) for i in range(cfg.H)]
+            if mul == 2:
+                xr = [_bf16(_f32(v * float(tw[t, j]))) for v in xr]
             h = []
             for n in range(cfg.N1):
-                s = _f32(math.fsum(float(x[t, i]) * W13[n][i] for i in range(cfg.H)))
+                s = _f32(math.fsum(xr[i] * W13[n][i] for i in range(cfg.H)))
                 if w13["gscale"] is not None:
                     s = _f32(s * float(w13["gscale"][e]))
                 if w13["bias"] is not None:
@@ -103,7 +108,7 @@ def _brute_layer(Lr, cfg, ids, tw, mul=True):
                     z = _f32(z * float(w2["gscale"][e]))
                 if w2["bias"] is not None:
                     z = _f32(z + float(w2["bias"][e][n]))
-                if mul:
+                if mul is True or mul == 1:
                     z = _f32(z * float(tw[t, j]))
                 row_out[n] = _f32(row_out[n] + _bf16(z)) if j else _bf16(z)
         out.append([_bf16(v) for v in row_out])
@@ -295,3 +300,35 @@ def test_unpadded_output_shape():
     r = L.moe_forward(Lr["x"], Lr["logits"], Lr["w13"], Lr["w2"], 2)
     assert r["out"].shape == (5, 192) and r["y"].shape[1] == 192
     assert r["out"].strides == (192 * 4, 4)
+
+
+@pytest.mark.parametrize("fmt,act,H,I", [
+    ("nvfp4", "swigluoai", 64, 64),
+    ("mxfp4", "relu2", 64, 128),
+    ("int4", "swigluoai", 128, 64),
+])
+def test_brute_force_routing_weight_on_input(fmt, act, H, I):
+    """mul_topk_weights = 2 (the weight applied to each routed row's input)
+    against the pure-Python loops, bit for bit; and the mode differs from the
+    output multiply (swigluoai and ReLU^2 are not linear)."""
+    cfg, Lr = tiny_layer(fmt, act, T=3, E=4, k=2, H=H, I=I)
+    a = L.ACT_SWIGLUOAI if act == "swigluoai" else L.ACT_RELU2
+    r = L.moe_forward(Lr["x"], Lr["logits"], Lr["w13"], Lr["w2"], cfg.k, act=a, mul_topk_weights=2)
+    bf = _brute_layer(Lr, cfg, r["topk_ids"], r["topk_weights"], mul=2)
+    assert np.array_equal(r["out"].view(np.uint32), bf.view(np.uint32))
+    r1 = L.moe_forward(Lr["x"], Lr["logits"], Lr["w13"], Lr["w2"], cfg.k, act=a, mul_topk_weights=True)
+    assert not np.array_equal(r["out"], r1["out"])
+    toks = L.moe_forward_tokens(Lr["x"], r["topk_ids"], r["topk_weights"], Lr["w13"], Lr["w2"],
+                                range(cfg.T), act=a, mul_topk_weights=2)
+    assert np.array_equal(toks.view(np.uint32), r["out"].view(np.uint32))
+
+
+def test_unit_weights_on_input_equal_no_weight():
+    """With every routing weight exactly 1 the input multiply is the identity:
+    on-input, on-output and no weighting give the same bits."""
+    cfg, Lr = tiny_layer("nvfp4", "swigluoai", T=4, E=4, k=2, H=64, I=64)
+    r0 = L.moe_forward(Lr["x"], Lr["logits"], Lr["w13"], Lr["w2"], cfg.k, mul_topk_weights=False)
+    ones = np.ones_like(r0["topk_weights"])
+    outs = [L.moe_forward(Lr["x"], None, Lr["w13"], Lr["w2"], cfg.k, mul_topk_weights=m,
+                          topk_ids=r0["topk_ids"], topk_weights=ones)["out"] for m in (0, 1, 2)]
+    assert all(np.array_equal(o.view(np.uint32), outs[0].view(np.uint32)) for o in outs)
