@@ -63,12 +63,19 @@ def read_peaks():
 
 
 def gemm_source_hash():
-    """Hash of the GEMM kernel sources, recorded beside each ncu summary."""
+    """Hash of what defines the grouped GEMM kernel (its source, the device
+    helpers it includes and its argument struct), recorded beside each ncu
+    summary: a summary whose hash differs was taken on other GEMM code."""
     import hashlib
+    import re
+    csrc = os.path.join(ROOT, "bit_block_scaled_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh", "kernels.h"):
-        with open(os.path.join(ROOT, "bit_block_scaled_gb300", "csrc", f), "rb") as fh:
+    for f in ("gemm.cu", "common.cuh", "dequant.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
+    with open(os.path.join(csrc, "kernels.h")) as fh:
+        args = re.search(r"struct GemmArgs \{.*?\};", fh.read(), flags=re.S)
+    h.update(args.group(0).encode())
     return h.hexdigest()[:16]
 
 

@@ -127,13 +127,25 @@ __device__ __forceinline__ uint4 interleave8(uint4 v) {
                     __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
 }
 
+// Routing weight applied on the input: bf16(fp32(x * w)) for both bf16 halves.
+__device__ __forceinline__ uint32_t weigh_bf16x2(uint32_t pair, float w) {
+  const uint32_t lo = float_to_bf16_bits(__fmul_rn(bf16_bits_to_float((uint16_t)(pair & 0xFFFFu)), w));
+  const uint32_t hi = float_to_bf16_bits(__fmul_rn(bf16_bits_to_float((uint16_t)(pair >> 16)), w));
+  return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint4 weigh8(uint4 q, float w) {
+  return make_uint4(weigh_bf16x2(q.x, w), weigh_bf16x2(q.y, w), weigh_bf16x2(q.z, w), weigh_bf16x2(q.w, w));
+}
+
 // x_perm[p] = x[sorted[p] / k] (columns interleaved within groups of 8), zero
 // for padding slots; slots past the last used one (offsets[E]) are never read
-// by the GEMMs and are skipped.
+// by the GEMMs and are skipped. With tw (routing weight on the input) each row
+// is bf16(x * tw[sorted[p]]), the routed row's own weight.
 __global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x, int R, int k, int H8,
                                                      const int32_t *__restrict__ sorted,
                                                      const int32_t *__restrict__ used_end,
-                                                     uint4 *__restrict__ x_perm) {
+                                                     uint4 *__restrict__ x_perm, const float *__restrict__ tw) {
   pdl_wait();
   pdl_trigger();
   const int p = blockIdx.x;
@@ -142,21 +154,27 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x
   uint4 *dst = x_perm + (size_t)p * H8;
   if (s >= 0 && s < R) {
     const uint4 *src = x + (size_t)(s / k) * H8;
-    for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = interleave8(src[v]);
+    if (tw) {
+      const float w = tw[s];
+      for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = interleave8(weigh8(src[v], w));
+    } else {
+      for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = interleave8(src[v]);
+    }
   } else {
     for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
   }
 }
 
 // f16 operand path: x16[p] = f16(x[sorted[p] / k] * 2^-e_p) in natural column
-// order, where e_p >= 0 is the smallest exponent that brings the row's largest
-// magnitude to at most 2^15, so every element fits f16 (the scaling is exact;
-// only elements below 2^-24 of the scaled row lose bits). xexp[p] = e_p; the
-// GEMM epilogue multiplies by 2^e_p. Padding slots get zeros and e_p = 0.
+// order, with e_p chosen below so the row's largest magnitude lands in
+// [2^14, 2^15) (exact for every bf16 element down to 2^-31 of it). xexp[p] =
+// e_p; the GEMM epilogue multiplies by 2^e_p. Padding slots get zeros and
+// e_p = 0. With tw the row is first weighted as in gather_kernel.
 __global__ void __launch_bounds__(128) gather_f16_kernel(const uint4 *__restrict__ x, int R, int k, int H8,
                                                          const int32_t *__restrict__ sorted,
                                                          const int32_t *__restrict__ used_end,
-                                                         uint4 *__restrict__ x16, int32_t *__restrict__ xexp) {
+                                                         uint4 *__restrict__ x16, int32_t *__restrict__ xexp,
+                                                         const float *__restrict__ tw) {
   __shared__ float wmax[4];
   pdl_wait();
   pdl_trigger();
@@ -170,9 +188,10 @@ __global__ void __launch_bounds__(128) gather_f16_kernel(const uint4 *__restrict
     return;
   }
   const uint4 *src = x + (size_t)(s / k) * H8;
+  const float rw = tw ? tw[s] : 1.f;
   float m = 0.f;
   for (int v = threadIdx.x; v < H8; v += blockDim.x) {
-    const uint4 q = src[v];
+    const uint4 q = tw ? weigh8(src[v], rw) : src[v];
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -191,7 +210,7 @@ __global__ void __launch_bounds__(128) gather_f16_kernel(const uint4 *__restrict
   const int e = max(-126, min(ex - 15, 126));
   const float sc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
   for (int v = threadIdx.x; v < H8; v += blockDim.x) {
-    const uint4 q = src[v];
+    const uint4 q = tw ? weigh8(src[v], rw) : src[v];
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     uint32_t o[4];
 #pragma unroll
@@ -208,11 +227,11 @@ __global__ void __launch_bounds__(128) gather_f16_kernel(const uint4 *__restrict
 
 moe_status_t launch_gather_f16(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
                                const int32_t *offsets_end, uint16_t *x16, int32_t *xexp, cudaStream_t stream,
-                               int *launches) {
+                               int *launches, const float *tw) {
   if (P_max == 0) return MOE_OK;
   const cudaError_t err = launch_pdl(gather_f16_kernel, dim3(P_max), dim3(128), 0, stream,
                                      reinterpret_cast<const uint4 *>(x), T * k, k, H / 8, sorted_ids, offsets_end,
-                                     reinterpret_cast<uint4 *>(x16), xexp);
+                                     reinterpret_cast<uint4 *>(x16), xexp, tw);
   if (launches) ++*launches;
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -227,11 +246,12 @@ moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, 
 }
 
 moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
-                           const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches) {
+                           const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches,
+                           const float *tw) {
   if (P_max == 0) return MOE_OK;
   const cudaError_t err = launch_pdl(gather_kernel, dim3(P_max), dim3(128), 0, stream,
                                      reinterpret_cast<const uint4 *>(x), T * k, k, H / 8, sorted_ids, offsets_end,
-                                     reinterpret_cast<uint4 *>(x_perm));
+                                     reinterpret_cast<uint4 *>(x_perm), tw);
   if (launches) ++*launches;
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

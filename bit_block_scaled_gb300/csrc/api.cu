@@ -212,8 +212,10 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
   if (!mark(1)) return MOE_ERR_CUDA;
   if ((s = launch_align(ids, T, k, E, bm, P, sorted, offs, blocks, rowpos, status, st, n)) != MOE_OK) return s;
   if (!mark(2)) return MOE_ERR_CUDA;
-  s = f16_1 ? launch_gather_f16(x, T, k, H, P, sorted, offs + E, xperm, xexp, st, n)
-          : launch_gather(x, T, k, H, P, sorted, offs + E, xperm, st, n);
+  // mul: 0 no routing weight, 1 in the GEMM2 epilogue, 2 on GEMM1's input rows
+  const float *tw_in = mul == 2 ? tw : nullptr;
+  s = f16_1 ? launch_gather_f16(x, T, k, H, P, sorted, offs + E, xperm, xexp, st, n, tw_in)
+          : launch_gather(x, T, k, H, P, sorted, offs + E, xperm, st, n, tw_in);
   if (s != MOE_OK) return s;
   if (!mark(3)) return MOE_ERR_CUDA;
   const int epi1 = act.kind == MOE_ACT_SWIGLUOAI ? 0 : 1;
@@ -222,7 +224,7 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
     return s;
   if (!mark(4)) return MOE_ERR_CUDA;
   moe_act_t none = {0, 0.f, 0.f};
-  if ((s = launch_grouped_gemm(2, *w2, abuf, P, sorted, offs, R, tw, mul ? 1 : 0, 0, none, ybuf, H, status, st,
+  if ((s = launch_grouped_gemm(2, *w2, abuf, P, sorted, offs, R, tw, mul == 1 ? 1 : 0, 0, none, ybuf, H, status, st,
                                n, f16_2)) != MOE_OK)
     return s;
   if (!mark(5)) return MOE_ERR_CUDA;
@@ -232,8 +234,9 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
 
 static moe_status_t check_forward(const float *sel_bias, int T, int E, int k, int H, int I, int route,
                                   const moe_qweight_t *w13, const moe_qweight_t *w2, int layout, moe_act_t act,
-                                  int *block_m, void *ws, size_t ws_bytes) {
+                                  int *block_m, void *ws, size_t ws_bytes, int mul) {
   if (*block_m == 0) *block_m = 16;
+  if (mul < 0 || mul > 2) return MOE_ERR_INVALID_ARG;  // routing weight: none, on the output, on the input
   if (!valid_dims(T, E, k, H, I) || !valid_block_m(*block_m)) return MOE_ERR_INVALID_ARG;
   if (route != MOE_ROUTE_TOPK_SOFTMAX && route != MOE_ROUTE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
   if (route == MOE_ROUTE_SIGMOID_BIAS && !aligned16(sel_bias)) return MOE_ERR_INVALID_ARG;
@@ -254,7 +257,7 @@ moe_status_t moe_forward(const uint16_t *x, const float *logits, const float *se
                          size_t ws_bytes, moe_stream_t stream) {
   g_last_launches = 0;
   moe_status_t s = check_forward(sel_bias, T, E, k, H, I, route, w13, w2, gate_up_layout, act, &block_m, ws,
-                                 ws_bytes);
+                                 ws_bytes, mul_topk_weights);
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
   if (!aligned16(x) || !aligned16(logits) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
@@ -269,7 +272,7 @@ moe_status_t moe_forward_profile(const uint16_t *x, const float *logits, const f
   g_last_launches = 0;
   if (!kernel_ms) return MOE_ERR_INVALID_ARG;
   moe_status_t s = check_forward(sel_bias, T, E, k, H, I, route, w13, w2, gate_up_layout, act, &block_m, ws,
-                                 ws_bytes);
+                                 ws_bytes, mul_topk_weights);
   if (s != MOE_OK) return s;
   for (int i = 0; i < 6; ++i) kernel_ms[i] = 0.f;
   if (T == 0) return MOE_OK;
@@ -297,7 +300,7 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *logits_host, 
                               int block_m, uint16_t *out_host, void *ws, size_t ws_bytes, moe_stream_t stream) {
   g_last_launches = 0;
   moe_status_t s = check_forward(sel_bias, T, E, k, H, I, route, w13, w2, gate_up_layout, act, &block_m, ws,
-                                 ws_bytes);
+                                 ws_bytes, mul_topk_weights);
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
   if (!x_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;

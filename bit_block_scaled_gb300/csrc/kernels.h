@@ -52,12 +52,15 @@ moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, 
                           int32_t *sorted_ids, int32_t *offsets, int32_t *block_ids, int32_t *row_pos,
                           unsigned int *status, cudaStream_t stream, int *launches);
 
+// tw (optional): the routing weight applied on the input, x row * tw[sorted[p]]
+// rounded to bf16 before it is gathered.
 moe_status_t launch_gather_f16(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
                                const int32_t *offsets_end, uint16_t *x16, int32_t *xexp, cudaStream_t stream,
-                               int *launches);
+                               int *launches, const float *tw = nullptr);
 
 moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
-                           const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches);
+                           const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches,
+                           const float *tw = nullptr);
 
 moe_status_t launch_unpermute(const uint16_t *y, const int32_t *row_pos, int T, int k, int H, int P_max,
                               uint16_t *out, unsigned int *status, cudaStream_t stream, int *launches);

@@ -202,7 +202,13 @@ moe_status_t moe_unpermute_reduce(const uint16_t *y, const int32_t *row_pos,
 /* Steps a1..a5 in order on one stream, intermediates in `ws` (ws_bytes >=
  * moe_workspace_size(T, E, k, H, I, block_m)). x bf16 [T][H], logits fp32
  * [T][E], out bf16 [T][H]. block_m = 0 picks 16. No host synchronisation:
- * the call can be captured in a CUDA graph. */
+ * the call can be captured in a CUDA graph.
+ * mul_topk_weights selects where each routed row's own routing weight w
+ * applies [MARLIN "Minimal repro": apply_router_weight_on_input]: 0 nowhere,
+ * 1 in the GEMM2 epilogue (z *= w, as moe_grouped_gemm2_weighted), 2 on the
+ * input (the row enters GEMM1 as bf16(x * w) and GEMM2 does not multiply);
+ * other values are MOE_ERR_INVALID_ARG. The same holds for the _host,
+ * _static and _profile variants. */
 moe_status_t moe_forward(const uint16_t *x, const float *logits,
                          const float *sel_bias, int T, int E, int k, int H,
                          int I, int route, const moe_qweight_t *w13,

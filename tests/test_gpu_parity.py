@@ -427,3 +427,28 @@ def test_fused_mxfp4_f16_scale_range():
     assert moe.moe_read_status(ws) == 0
     o = oracle_full(N, cfg)
     assert_close(out.float().cpu().numpy(), o["out"], "mxfp4 f16 path, extreme scales")
+
+
+@pytest.mark.parametrize("fmt,act", [("nvfp4", "swigluoai"), ("mxfp4", "relu2"), ("int4", "swigluoai"),
+                                     ("mxfp4", "swigluoai")])
+def test_routing_weight_on_input(fmt, act):
+    """mul_topk_weights = 2: each routed row enters GEMM1 as bf16(x * w) with
+    its own routing weight and GEMM2 does not multiply (bf16 and f16 gathers)."""
+    import bit_block_scaled_gb300 as moe
+    cfg = get_config("c0", name=f"on_input_{fmt}_{act}", fmt=fmt, act=act, H=320, I=256, E=8, T=37, k=3)
+    L, N = make(cfg, seed=31)
+    g = gpu_steps(L, cfg)
+    ws = torch.zeros(moe.moe_workspace_size(cfg.T, cfg.E, cfg.k, cfg.H, cfg.I, 16), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(L["x"], L["logits"], L["sel_bias"], cfg.k, moe.ROUTE[cfg.route], L["w13"], L["w2"], 0,
+                    act_of(cfg), 2, 16, out, ws)
+    assert moe.moe_read_status(ws) == 0
+    o = oracle_full(N, cfg, ids=g["topk_ids"].astype(np.int32), tw=g["topk_weights"], mul=2)
+    assert_close(out.float().cpu().numpy(), o["out"], f"on-input out ({fmt}, {act})")
+    o1 = oracle_full(N, cfg, ids=g["topk_ids"].astype(np.int32), tw=g["topk_weights"], mul=True)
+    assert not np.allclose(o["out"], o1["out"])  # the two settings really differ here
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(L["x"], L["logits"], L["sel_bias"], cfg.k, moe.ROUTE[cfg.route], L["w13"], L["w2"], 0,
+                        act_of(cfg), 3, 16, out, ws)
+    assert e.value.code == 1
