@@ -44,6 +44,7 @@
 //    from bf16-pair FMAs (the fp16 scale split into two bf16 parts).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -678,26 +679,39 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Per-device host caches: devices are numbered below kMaxDevices.
+constexpr int kMaxDevices = 64;
+constexpr uint32_t kMaxSmem = 227 * 1024;  // dynamic shared memory a CTA may opt into
+
+int current_device() {
+  int dev = 0;
+  return (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) ? dev : 0;
+}
+
+// SM count of the current device (queried once per device).
 int sm_count() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-  });
+  static std::atomic<int> cached[kMaxDevices];
+  const int dev = current_device();
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
   return n;
 }
 
 template <int FMT, int EPI, int KPB, bool F16>
 moe_status_t launch_t(const GemmArgs &a, dim3 grid, uint32_t smem, cudaStream_t st) {
   auto kern = grouped_gemm_kernel<FMT, EPI, KPB, F16>;
-  static uint32_t configured = 0;  // per instantiation; grows monotonically
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  // the dynamic shared-memory limit is a per-device function attribute: set
+  // it once per device to the most any launch asks for (every thread writes
+  // the same value, so racing first launches agree)
+  static std::atomic<int> configured[kMaxDevices];
+  std::atomic<int> &done = configured[current_device()];
+  if (!done.load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) != cudaSuccess)
       return MOE_ERR_CUDA;
-    configured = smem;
+    done.store(1, std::memory_order_release);
   }
   return launch_pdl(kern, grid, dim3(kThreads), smem, st, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -810,7 +824,7 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   uint32_t smem = smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes).total;
   // one CTA per SM: it allocates all of TMEM
   if (smem < 120 * 1024) smem = 120 * 1024;
-  if (smem > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+  if (smem > kMaxSmem) return MOE_ERR_UNSUPPORTED;
   // persistent grid: one wave of resident CTAs, at most one per possible tile
   const int active = num_rows < E ? num_rows : E;
   const int max_tiles = a.m_tiles * (P_max / a.tile_n + active + 1);
