@@ -452,3 +452,20 @@ def test_routing_weight_on_input(fmt, act):
         moe.moe_forward(L["x"], L["logits"], L["sel_bias"], cfg.k, moe.ROUTE[cfg.route], L["w13"], L["w2"], 0,
                         act_of(cfg), 3, 16, out, ws)
     assert e.value.code == 1
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "int4"])
+def test_maximum_sizes(fmt):
+    """The largest sizes the ABI accepts: 256 experts with top-8 routing, and
+    H = I = 4096 (256-byte NVFP4 scale rows, 16 K stages of 256 per tile),
+    each through the steps and the fused forward."""
+    import bit_block_scaled_gb300 as moe
+    for name, T, E, k, H, I in (("maxE", 40, 256, 8, 128, 128), ("maxH", 9, 2, 2, 4096, 4096)):
+        cfg = get_config("c0", name=f"{name}_{fmt}", fmt=fmt, T=T, E=E, k=k, H=H, I=I)
+        L, N = make(cfg, seed=41)
+        g = gpu_steps(L, cfg)
+        o = oracle_full(N, cfg)
+        _check_steps(g, o, cfg)
+        out, ws = gpu_forward(L, cfg)
+        assert moe.moe_read_status(ws) == 0
+        assert_close(out.float().cpu().numpy(), o["out"], f"fused out {name} {fmt}")
