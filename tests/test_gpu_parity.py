@@ -78,6 +78,7 @@ FORMATS = [
     ("nvfp4", "swigluoai", 320, 192, 5, 37, 2, 1),
     ("nvfp4", "relu2", 192, 320, 6, 29, 3, 0),
     ("mxfp4", "swigluoai", 384, 256, 4, 41, 2, 0),
+    ("mxfp4", "swigluoai", 384, 256, 4, 41, 2, 1),
     ("mxfp4", "relu2", 256, 192, 7, 23, 2, 0),
     ("int4", "swigluoai", 320, 256, 5, 33, 2, 0),
     ("int4", "relu2", 448, 192, 4, 19, 3, 0),
@@ -86,6 +87,7 @@ FORMATS = [
 
 @pytest.mark.parametrize("fmt,act,H,I,E,T,k,layout", FORMATS)
 def test_formats_and_activations(fmt, act, H, I, E, T, k, layout):
+    import bit_block_scaled_gb300 as moe
     route = "sigmoid_bias" if act == "relu2" else "topk_softmax"
     cfg = get_config("c0", name=f"fmt_{fmt}_{act}_{H}_{I}", fmt=fmt, act=act, H=H, I=I, E=E, T=T,
                      k=k, route=route, sel_bias_std=0.1 if route == "sigmoid_bias" else 0.0,
@@ -112,6 +114,10 @@ def test_formats_and_activations(fmt, act, H, I, E, T, k, layout):
     np.testing.assert_allclose(g["topk_weights"], oref["topk_weights"], rtol=2e-6, atol=1e-7) \
         if np.array_equal(ids, oref["topk_ids"]) else None
     _check_steps(g, o, cfg, exact_routing=False)
+    # the fused forward (f16 operands for NVFP4 / MXFP4) in the same layout
+    out, ws = gpu_forward(L, cfg, layout=layout)
+    assert moe.moe_read_status(ws) == 0
+    assert_close(out.float().cpu().numpy(), o["out"], f"fused out ({fmt}, {act}, layout {layout})")
 
 
 def test_c1_decode_layer_full():
