@@ -6,8 +6,15 @@ Distributions follow the stated workloads: activations bf16 N(0, 1); router
 logits fp32 N(0, 1) (plus -zipf * ln(e + 1) for the skewed workload); expert
 weights fp32 N(0, 0.02) quantised to the workload's 4-bit format; biases bf16
 N(0, 0.01); the selection bias of sigmoid routing fp32 N(0, 0.1).
+
+Every tensor is drawn by a torch CPU generator and quantised on the CPU;
+only the finished bytes are copied to ``device``. The layer is therefore the
+same bytes whichever device it is made for, and making it launches no GPU
+work beyond the copies.
 """
+import os
 import zlib
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -20,15 +27,17 @@ def _seed(*parts) -> int:
     return zlib.crc32("|".join(str(p) for p in parts).encode()) & 0x7FFFFFFF
 
 
-def _gen(device, *parts) -> torch.Generator:
-    g = torch.Generator(device=device)
+def _gen(*parts) -> torch.Generator:
+    g = torch.Generator(device="cpu")
     g.manual_seed(_seed(*parts))
     return g
 
 
 def randn(shape, std, device, *parts) -> torch.Tensor:
-    return torch.randn(shape, generator=_gen(device, *parts), device=device,
-                       dtype=torch.float32) * std
+    """N(0, std^2) fp32 drawn on the CPU from the generator of ``parts``, then
+    copied to ``device``."""
+    t = torch.randn(shape, generator=_gen(*parts), dtype=torch.float32) * std
+    return t.to(device)
 
 
 def make_projection(cfg: LayerConfig, which: str, N: int, K: int, seed: int,
@@ -46,37 +55,47 @@ def make_projection(cfg: LayerConfig, which: str, N: int, K: int, seed: int,
     else:
         out["scales"] = torch.empty((E, N, K // 64), dtype=torch.float16, device=device)
         out["zeros"] = torch.empty((E, N, (K // 64 + 1) // 2), dtype=torch.uint8, device=device)
-    for e in range(E) if experts is None else experts:
-        w = randn((N, K), cfg.w_std, device, seed, cfg.name.split("_t")[0], which, e)
+    def draw(e):
+        # drawn and quantised on the host (one generator per expert, so the
+        # bytes do not depend on the order or the thread that makes them)
+        w = randn((N, K), cfg.w_std, "cpu", seed, cfg.name.split("_t")[0], which, e)
         if fmt == 0:
-            pq, sc, gs = qz.quantize_nvfp4(w)
-            out["gscale"][e] = gs
-        elif fmt == 1:
-            pq, sc = qz.quantize_mxfp4(w)
-        else:
-            pq, sc, zz = qz.quantize_int4(w)
-            out["zeros"][e] = zz
-        q[e] = pq
-        out["scales"][e] = sc
-        del w
+            return qz.quantize_nvfp4(w)
+        if fmt == 1:
+            return qz.quantize_mxfp4(w)
+        return qz.quantize_int4(w)
+
+    todo = list(range(E) if experts is None else experts)
+    with ThreadPoolExecutor(max(1, min(8, os.cpu_count() or 1))) as pool:
+        for e, res in zip(todo, pool.map(draw, todo)):
+            # the finished bytes go to the device
+            if fmt == 0:
+                pq, sc, gs = res
+                out["gscale"][e] = gs
+            elif fmt == 1:
+                pq, sc = res
+            else:
+                pq, sc, zz = res
+                out["zeros"][e] = zz
+            q[e] = pq
+            out["scales"][e] = sc
     if with_bias:
-        out["bias"] = randn((E, N), cfg.bias_std, device, seed, cfg.name.split("_t")[0],
-                            which + "_bias").to(torch.bfloat16)
+        out["bias"] = randn((E, N), cfg.bias_std, "cpu", seed, cfg.name.split("_t")[0],
+                            which + "_bias").to(torch.bfloat16).to(device)
     return out
 
 
 def make_activations(cfg: LayerConfig, seed: int, device="cpu") -> dict:
     base = cfg.name.split("_t")[0]
-    x = randn((cfg.T, cfg.H), cfg.x_std, device, seed, cfg.name, "x").to(torch.bfloat16)
-    logits = randn((cfg.T, cfg.E), 1.0, device, seed, cfg.name, "logits")
+    x = randn((cfg.T, cfg.H), cfg.x_std, "cpu", seed, cfg.name, "x").to(torch.bfloat16)
+    logits = randn((cfg.T, cfg.E), 1.0, "cpu", seed, cfg.name, "logits")
     if cfg.zipf:
-        prior = -cfg.zipf * torch.log(torch.arange(1, cfg.E + 1, device=device,
-                                                   dtype=torch.float32))
+        prior = -cfg.zipf * torch.log(torch.arange(1, cfg.E + 1, dtype=torch.float32))
         logits = logits + prior[None, :]
     sel_bias = None
     if cfg.route == "sigmoid_bias":
-        sel_bias = randn((cfg.E,), cfg.sel_bias_std, device, seed, base, "sel_bias")
-    return dict(x=x, logits=logits.contiguous(), sel_bias=sel_bias)
+        sel_bias = randn((cfg.E,), cfg.sel_bias_std, "cpu", seed, base, "sel_bias").to(device)
+    return dict(x=x.to(device), logits=logits.contiguous().to(device), sel_bias=sel_bias)
 
 
 def make_layer(cfg: LayerConfig, seed: int = 0, device="cpu", weights=True) -> dict:

@@ -13,8 +13,9 @@ workload recipe, with the readings noted where the recipe leaves a step open:
 * GPTQ INT4 (asymmetric min/max, group 64 along K): s = fp16((max-min)/15)
   (0 becomes 1), z = clamp(rne(-min/s), 0, 15), q = clamp(rne(w/s) + z, 0, 15).
 
-All arithmetic is fp32 torch ops (CPU or CUDA), so the same call gives the
-same bytes on either device.
+All arithmetic is fp32 torch ops on the CPU: the layer generator draws and
+quantises every tensor on the host and copies the bytes to the device, so the
+GPU runs, the oracle and the timed CPU baseline all read the same bytes.
 """
 import torch
 
@@ -47,8 +48,21 @@ def _nearest_even_code(mag: torch.Tensor, grid) -> torch.Tensor:
     return idx.to(torch.uint8)
 
 
+# E2M1 decision points between neighbouring magnitudes (0, .5, 1, 1.5, 2, 3,
+# 4, 6): the midpoints, each with the side an exact tie goes to (the even
+# code). A magnitude takes the code equal to the number of points it passes.
+_E2M1_MIDS = [(0.25, False), (0.75, True), (1.25, False), (1.75, True), (2.5, False),
+              (3.5, True), (5.0, False)]  # (midpoint, tie goes up)
+
+
 def e2m1_encode(x: torch.Tensor) -> torch.Tensor:
-    code = _nearest_even_code(x.abs(), _E2M1_POS)
+    """fp32 -> E2M1 code (nearest, ties to the even code, saturating at 6;
+    the sign bit follows x). Same decisions as the grid search of
+    ``_nearest_even_code`` (pinned by a test), as seven comparisons."""
+    mag = x.abs()
+    code = torch.zeros(x.shape, dtype=torch.uint8)
+    for mid, up in _E2M1_MIDS:
+        code += (mag >= mid) if up else (mag > mid)
     return code | (torch.signbit(x).to(torch.uint8) << 3)
 
 

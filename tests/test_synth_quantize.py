@@ -76,3 +76,16 @@ def test_int4_quantiser_invariants():
     err = np.abs(deq - w.double().numpy())
     assert np.all(err <= sv * 0.5 + np.abs(w.double().numpy()) * 2 ** -8 + 1e-12)
     assert np.all(deq[3, 64:128] == 0.0)
+
+
+def test_e2m1_encode_comparisons_equal_grid_search():
+    """The comparison form of the E2M1 encoder takes the same decisions as the
+    nearest-value grid search with ties to the even code, on every exact
+    midpoint, its neighbours one fp32 ulp away, and random magnitudes."""
+    mids = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], dtype=torch.float32)
+    pts = torch.cat([mids, torch.nextafter(mids, torch.tensor(0.0)), torch.nextafter(mids, torch.tensor(10.0)),
+                     torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 6.5, 1e30, float("inf")]),
+                     torch.rand(50000, generator=torch.Generator().manual_seed(3)) * 8])
+    x = torch.cat([pts, -pts])
+    ref = Q._nearest_even_code(x.abs(), Q._E2M1_POS) | (torch.signbit(x).to(torch.uint8) << 3)
+    assert torch.equal(Q.e2m1_encode(x), ref)
