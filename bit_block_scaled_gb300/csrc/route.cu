@@ -6,6 +6,14 @@
 // SIGMOID_BIAS (Nemotron-3-Nano; vLLM issue "... non-gated ReLU2 MoE
 // (Nemotron-3-Nano)", Analysis item 3, n_group = 1): s = sigmoid(logit) in
 // fp32, select by s + bias, weights = selected s renormalised to sum 1.
+//
+// Non-finite scores (the pages say nothing about them; the reading taken):
+// a NaN selection score ranks as -inf, and equal scores (two -inf included)
+// go to the lower expert id. The softmax weights are exp(l_j - max) when the
+// largest selected logit is finite; when it is +inf or -inf, the selected
+// logits equal to it share the weight equally (the limit of the softmax) and
+// the rest get 0. A NaN logit weighs as -inf. Sigmoid routing weighs a NaN
+// logit as s = 0; if every selected s is 0 the k weights are 1/k each.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -69,7 +77,13 @@ __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restr
     }
     if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
     sel_id[j] = bid;
-    sel_v[j] = (ROUTE == MOE_ROUTE_SIGMOID_BIAS) ? sigmoid_f32(row[bid]) : best;
+    if (ROUTE == MOE_ROUTE_SIGMOID_BIAS) {
+      const float sv = sigmoid_f32(row[bid]);
+      sel_v[j] = sv != sv ? 0.f : sv;  // a NaN logit weighs as s = 0
+    } else {
+      const float l = row[bid];
+      sel_v[j] = l != l ? -INFINITY : l;  // a NaN logit weighs as -inf
+    }
   }
   if (lane != 0) return;
   float w[kMaxK];
@@ -81,12 +95,22 @@ __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restr
         w[j] = sel_v[j];
         sum += w[j];
       }
+    if (sum == 0.f) {  // every selected s is 0: equal weights
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) w[j] = 1.f;
+      sum = (float)k;
+    }
   } else {
-    const float m = sel_v[0];
+    // the slots hold descending scores, so slot 0 has the largest logit
+    float m = sel_v[0];
+#pragma unroll
+    for (int j = 1; j < kMaxK; ++j)
+      if (j < k) m = fmaxf(m, sel_v[j]);
+    const bool finite = fabsf(m) <= 3.402823466e38f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j)
       if (j < k) {
-        w[j] = expf(sel_v[j] - m);
+        w[j] = finite ? expf(sel_v[j] - m) : (sel_v[j] == m ? 1.f : 0.f);
         sum += w[j];
       }
   }

@@ -134,3 +134,40 @@ def test_gather_rows_pads_with_zero():
     assert xp.shape == (12, 4)
     assert np.array_equal(xp[0], x[0]) and np.array_equal(xp[1], x[2])
     assert np.all(xp[2] == 0) and np.array_equal(xp[8], x[1])
+
+
+def test_non_finite_logits_rank_and_weigh_by_their_limits():
+    """Closed forms of the non-finite reading: NaN ranks as -inf (ties with
+    -inf go to the lower id); a +inf or -inf maximum splits the weight equally
+    among the selected logits equal to it; a NaN logit weighs as -inf."""
+    nan, inf = np.nan, np.inf
+    logits = np.array([[nan, -inf, 0.0, 1.0],      # NaN and -inf tie at -inf: id 0 first
+                       [nan, nan, nan, nan],       # all NaN: ids 0, 1, 2; equal weights
+                       [inf, 0.0, inf, 1.0],       # two +inf share the weight
+                       [-inf, -inf, -inf, -inf],   # all -inf: equal weights
+                       [2.0, nan, 2.0, -inf]], np.float32)
+    ids, w = R.topk_softmax(logits, 3)
+    assert ids.tolist() == [[3, 2, 0], [0, 1, 2], [0, 2, 3], [0, 1, 2], [0, 2, 1]]
+    e = np.exp(1.0)
+    np.testing.assert_array_equal(w[0], np.float32([e / (e + 1), 1 / (e + 1), 0.0]))
+    assert w[1].tolist() == [np.float32(1 / 3)] * 3
+    assert w[2].tolist() == [0.5, 0.5, 0.0]
+    assert w[3].tolist() == [np.float32(1 / 3)] * 3
+    assert w[4].tolist() == [0.5, 0.5, 0.0]
+    assert np.all(np.isfinite(w))
+
+
+def test_non_finite_logits_sigmoid_routing():
+    """Sigmoid routing: NaN scores rank as -inf; a NaN logit weighs as s = 0
+    (sigmoid(-inf)); selected scores that are all 0 give equal weights."""
+    nan, inf = np.nan, np.inf
+    logits = np.array([[nan, 0.0, -inf, inf],
+                       [nan, nan, -inf, -inf],
+                       [-inf, -inf, -inf, -inf]], np.float32)
+    bias = np.zeros(4, np.float32)
+    ids, w = R.sigmoid_bias_topk(logits, bias, 2)
+    # row 0: scores [-inf(NaN), 0.5, 0, 1] -> ids 3, 1; weights 1/(1+0.5), 0.5/1.5
+    assert ids.tolist() == [[3, 1], [2, 3], [0, 1]]
+    np.testing.assert_array_equal(w[0], np.float32([1 / 1.5, 0.5 / 1.5]))
+    assert w[1].tolist() == [0.5, 0.5]
+    assert w[2].tolist() == [0.5, 0.5]
