@@ -17,7 +17,8 @@ path follows as well:
   R0  the bf16 weight operand: NVFP4 E2M1*E4M3 (exact in bf16; the per-expert
       fp32 global scale multiplies the accumulator), MXFP4 E2M1*2^(e-127)
       (exact), GPTQ INT4 bf16_rne((q - z) * s_fp16);
-  --  accumulation over K in float64 (rounded once to fp32); then
+  --  accumulation over K in float64 (rounded once to fp32; ``acc_dtype``
+      float32 sums in fp32 instead, for the timed CPU baseline); then
       h = fp32(fp32(acc * gscale) + bias);
   R1  the activation output a is rounded to bf16;
   R2  GEMM2: z = fp32(fp32(acc * gscale) + b2); z = fp32(z * w_row) when the
@@ -136,10 +137,17 @@ def bias_of(w: dict, e: int):
 
 
 # ------------------------------------------------------------------ GEMM pieces
-def matvec_rows(W: np.ndarray, X: np.ndarray) -> np.ndarray:
-    """acc[i, n] = sum_k X[i, k] * W[n, k] in float64, one row at a time (the
+def matvec_rows(W: np.ndarray, X: np.ndarray, acc_dtype=np.float64) -> np.ndarray:
+    """acc[i, n] = sum_k X[i, k] * W[n, k], rounded to fp32.
+
+    acc_dtype float64 (parity mode): summed in float64 one row at a time (the
     same call per row whatever the batching, so results do not depend on how
-    rows are grouped), rounded once to fp32."""
+    rows are grouped), rounded once to fp32. acc_dtype float32 (the timed CPU
+    baseline): one float32 matrix product over all rows; the operands are the
+    same values (bf16 activations and R0 weights are exact in fp32), only the
+    summation precision and order differ."""
+    if np.dtype(acc_dtype) == np.float32:
+        return np.asarray(X, dtype=np.float32) @ np.asarray(W, dtype=np.float32).T
     X = np.asarray(X, dtype=np.float64)
     out = np.empty((X.shape[0], W.shape[0]), dtype=np.float64)
     for i in range(X.shape[0]):
@@ -181,9 +189,10 @@ def relu2(h: np.ndarray) -> np.ndarray:
     return f32(r * r)
 
 
-def expert_gemm1_act(x_rows, W13, gscale, bias, act, layout, alpha=1.702, limit=7.0):
+def expert_gemm1_act(x_rows, W13, gscale, bias, act, layout, alpha=1.702, limit=7.0,
+                     acc_dtype=np.float64):
     """Rows routed to one expert: x_rows [n, H] (bf16 values) -> a [n, I] bf16."""
-    h = linear_epilogue(matvec_rows(W13, x_rows), gscale, bias)
+    h = linear_epilogue(matvec_rows(W13, x_rows, acc_dtype), gscale, bias)
     if act == ACT_SWIGLUOAI:
         g, u = gate_up_split(h, layout)
         a = swigluoai(g, u, alpha, limit)
@@ -194,10 +203,10 @@ def expert_gemm1_act(x_rows, W13, gscale, bias, act, layout, alpha=1.702, limit=
     return bf16_rne(a)                                              # R1
 
 
-def expert_gemm2(a_rows, W2, gscale, bias, row_weights=None):
+def expert_gemm2(a_rows, W2, gscale, bias, row_weights=None, acc_dtype=np.float64):
     """Rows of one expert: a_rows [n, I] -> y [n, H] bf16; row_weights [n] fp32
     multiplies each row by its own routing weight (the epilogue multiply)."""
-    z = linear_epilogue(matvec_rows(W2, a_rows), gscale, bias)
+    z = linear_epilogue(matvec_rows(W2, a_rows, acc_dtype), gscale, bias)
     if row_weights is not None:
         z = f32(z.astype(np.float64) * np.asarray(row_weights, np.float64)[:, None])
     return bf16_rne(z)                                              # R2
@@ -217,9 +226,10 @@ def unpermute_reduce(y: np.ndarray, row_pos: np.ndarray, T: int, k: int) -> np.n
 
 # ------------------------------------------------------------------- the layer
 def grouped_gemm1_act(x_perm, expert_offsets, sorted_token_ids, num_rows, w13,
-                      act, layout, alpha=1.702, limit=7.0):
-    """Step a3b over all experts. Rows of x_perm that hold padding (sorted id
-    >= num_rows) are left at zero in the result."""
+                      act, layout, alpha=1.702, limit=7.0, acc_dtype=np.float64):
+    """Step a3b over all experts, streamed one expert at a time (each expert's
+    weights are dequantised once, used for its rows and dropped). Rows of
+    x_perm that hold padding (sorted id >= num_rows) are left at zero."""
     E = len(expert_offsets) - 1
     N1 = w13["q"].shape[1]
     I = N1 // 2 if act == ACT_SWIGLUOAI else N1
@@ -233,13 +243,14 @@ def grouped_gemm1_act(x_perm, expert_offsets, sorted_token_ids, num_rows, w13,
             continue
         W = dequant(w13, e)
         a[slots] = expert_gemm1_act(x_perm[slots], W, gscale_of(w13, e),
-                                    bias_of(w13, e), act, layout, alpha, limit)
+                                    bias_of(w13, e), act, layout, alpha, limit, acc_dtype)
     return a
 
 
 def grouped_gemm2_weighted(a, expert_offsets, sorted_token_ids, num_rows, w2,
-                           topk_weights_flat, mul_topk_weights):
-    """Step a4 over all experts; padding slots are left at zero. The routing
+                           topk_weights_flat, mul_topk_weights, acc_dtype=np.float64):
+    """Step a4 over all experts, streamed one expert at a time; padding slots
+    are left at zero. The routing
     weight of slot p is topk_weights_flat[sorted_token_ids[p]] -- the row's own
     flat index (the failure in the vLLM issue "moe_wna16_marlin_gemm applies
     wrong per-row topk weights" was reading another row's entry)."""
@@ -256,17 +267,19 @@ def grouped_gemm2_weighted(a, expert_offsets, sorted_token_ids, num_rows, w2,
             continue
         W = dequant(w2, e)
         rw = tw[s[slots]] if mul_topk_weights == MUL_OUTPUT else None
-        y[slots] = expert_gemm2(a[slots], W, gscale_of(w2, e), bias_of(w2, e), rw)
+        y[slots] = expert_gemm2(a[slots], W, gscale_of(w2, e), bias_of(w2, e), rw, acc_dtype)
     return y
 
 
 def moe_forward(x, logits, w13, w2, k, route_mode=_routing.ROUTE_TOPK_SOFTMAX,
                 sel_bias=None, act=ACT_SWIGLUOAI, layout=LAYOUT_INTERLEAVED,
                 alpha=1.702, limit=7.0, mul_topk_weights=True, block_m=16,
-                topk_ids=None, topk_weights=None):
+                topk_ids=None, topk_weights=None, acc_dtype=np.float64):
     """Steps a1..a5 in order; returns every intermediate. ``topk_ids`` /
     ``topk_weights`` may be given to skip routing (e.g. to feed another
-    implementation's routing decisions downstream)."""
+    implementation's routing decisions downstream). ``acc_dtype``: float64
+    accumulation for parity (the default), float32 for the timed CPU
+    baseline (see ``matvec_rows``)."""
     x = np.asarray(x, dtype=np.float32)
     T, H = x.shape
     E = w13["q"].shape[0]
@@ -283,9 +296,9 @@ def moe_forward(x, logits, w13, w2, k, route_mode=_routing.ROUTE_TOPK_SOFTMAX,
         x_perm = x_perm.copy()
         x_perm[used] = weight_rows_on_input(x_perm[used], topk_weights.reshape(-1)[srt[used]])
     a = grouped_gemm1_act(x_perm, meta["expert_offsets"], meta["sorted_token_ids"],
-                          R, w13, act, layout, alpha, limit)
+                          R, w13, act, layout, alpha, limit, acc_dtype)
     y = grouped_gemm2_weighted(a, meta["expert_offsets"], meta["sorted_token_ids"],
-                               R, w2, topk_weights.reshape(-1), mul_topk_weights)
+                               R, w2, topk_weights.reshape(-1), mul_topk_weights, acc_dtype)
     out = unpermute_reduce(y, meta["row_pos"], T, k)
     return dict(topk_ids=topk_ids, topk_weights=topk_weights, x_perm=x_perm,
                 a=a, y=y, out=out, **meta)
