@@ -79,6 +79,14 @@ def gemm_source_hash():
     return h.hexdigest()[:16]
 
 
+def workload_config(cfg, args, world):
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": cfg.workload, "name": args.config, "T": cfg.T, "E": cfg.E, "top_k": cfg.k,
+            "H": cfg.H, "I": cfg.I, "format": cfg.fmt, "activation": cfg.act, "route": cfg.route,
+            "block_m": args.block_m, "parallelism": f"replicas x{world}",
+            "l2": "flushed (256 MiB write) before every GPU step"}
+
+
 def operand_dtype(cfg):
     """The tensor-core operand type each GEMM of the fused forward uses.
     NVFP4 expands exactly to f16 (E2M1 value times E4M3 scale); its GEMM1 runs
@@ -196,11 +204,168 @@ def dist_env():
 
 
 # --------------------------------------------------------------- our arm (GPU)
+_PROJ_CACHE = {}
+
+
+def layer_for(cfg, seed, device):
+    """make_layer, with each projection made once per base workload and seed
+    (the c3 sweep's three token counts share one set of weights)."""
+    from synth.gen import make_activations, make_projection
+    d = make_activations(cfg, seed, device)
+    base = cfg.name.split("_t")[0]
+    for which, N, K in (("w13", cfg.N1, cfg.H), ("w2", cfg.H, cfg.I)):
+        key = (base, which, seed, device)
+        if key not in _PROJ_CACHE:
+            _PROJ_CACHE[key] = make_projection(cfg, which, N, K, seed, device, cfg.bias)
+        d[which] = _PROJ_CACHE[key]
+    d["cfg"] = cfg
+    return d
+
+
+class Layer:
+    """One workload's inputs, workspace and output on the device, plus a CUDA
+    graph of one moe_forward over them."""
+
+    def __init__(self, moe, cfg, seed, block_m, stream):
+        import torch
+        self.moe, self.cfg, self.bm, self.stream = moe, cfg, block_m, stream
+        self.L = layer_for(cfg, seed, "cuda")
+        T, E, k, H, I = cfg.T, cfg.E, cfg.k, cfg.H, cfg.I
+        self.ws = torch.zeros(moe.moe_workspace_size(T, E, k, H, I, block_m), dtype=torch.uint8, device="cuda")
+        self.out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+        self.q13, self.q2 = moe.qweight(self.L["w13"]), moe.qweight(self.L["w2"])
+        self.act = moe.act(cfg.act, cfg.alpha, cfg.limit)
+        self.route = moe.ROUTE[cfg.route]
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                self.fwd()
+        torch.cuda.synchronize()
+        self.launches = moe.moe_last_launch_count()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(self.graph, stream=stream):
+                self.fwd()
+        torch.cuda.synchronize()
+        moe.moe_clear_status(self.ws, stream)
+
+    def fwd(self):
+        L = self.L
+        self.moe.moe_forward(L["x"], L["logits"], L["sel_bias"], self.cfg.k, self.route, self.q13, self.q2, 0,
+                             self.act, 1, self.bm, self.out, self.ws, self.stream)
+
+    def status(self):
+        return self.moe.moe_read_status(self.ws, self.stream)
+
+    def routing_ids(self):
+        import torch
+        cfg = self.cfg
+        ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device="cuda")
+        tw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device="cuda")
+        ws = torch.zeros(self.moe._lib.STATUS_BYTES, dtype=torch.uint8, device="cuda")
+        self.moe.moe_route_topk(self.L["logits"], self.L["sel_bias"], cfg.k, self.route, ids, tw, ws, self.stream)
+        torch.cuda.synchronize()
+        return ids.cpu().numpy()
+
+
+def timed_loop(stream, flush, n, run):
+    """n steps, each timed with CUDA events on `stream`; L2 flushed (untimed)
+    before every step. Returns the per-step device times in ms."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            flush.zero_()
+            starts[i].record(stream)
+            run()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+
+
+def breakdown(layer, flush, iters):
+    """Median device time of each of moe_forward's six kernels, as the forward
+    runs them (moe_forward_profile: CUDA events around each launch on the
+    stream; L2 flushed before each pass)."""
+    import torch
+    moe, cfg, L = layer.moe, layer.cfg, layer.L
+    res = {}
+    with torch.cuda.stream(layer.stream):
+        for it in range(iters + 3):
+            flush.zero_()
+            ms = moe.moe_forward_profile(L["x"], L["logits"], L["sel_bias"], cfg.k, layer.route, layer.q13,
+                                         layer.q2, 0, layer.act, 1, layer.bm, layer.out, layer.ws, layer.stream)
+            if it >= 3:
+                for name, v in ms.items():
+                    res.setdefault(name, []).append(v)
+    med = {name: statistics.median(v) for name, v in res.items()}
+    return {"route_ms": med["route"], "align_gather_ms": med["align"] + med["gather"],
+            "gemm1_ms": med["gemm1"], "gemm2_ms": med["gemm2"], "unpermute_ms": med["unpermute"]}
+
+
+def roofline_of(cfg, ids, ms_layer, bd, peaks, peak_src, args_config):
+    """Roofline of the dominant kernel (GEMM1) and of the whole layer: HBM for
+    decode shapes (bytes bound), bf16 tensor peak for prefill shapes."""
+    ab = algorithmic_bytes(cfg, ids)
+    flops = algorithmic_flops(cfg)
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    decode = flops / (tc * 1e12) < ab["total"] / (hbm * 1e9)
+    g1 = bd["gemm1_ms"] / 1e3
+    traffic, _ = read_traffic(f"gemm1_{args_config}")
+    if decode:
+        g1_bytes = ab["w13"] + cfg.T * cfg.k * (cfg.H + cfg.I) * 2
+        achieved = g1_bytes / g1 / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": traffic,
+                "kernel": "grouped_gemm_kernel (GEMM1 + act)", "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": int(g1_bytes)}
+        layer_frac = ab["total"] / (hbm * 1e9) / (ms_layer / 1e3)
+    else:
+        g1_flops = 2 * cfg.T * cfg.k * cfg.N1 * cfg.H
+        achieved = g1_flops / g1 / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc, "unit": "TFLOP/s",
+                "frac": round(achieved / tc, 4), "traffic": traffic,
+                "kernel": "grouped_gemm_kernel (GEMM1 + act)", "peak_source": peak_src,
+                "algorithmic_flops_per_launch": int(g1_flops)}
+        layer_frac = flops / (tc * 1e12) / (ms_layer / 1e3)
+    return roof, layer_frac, ab, flops, decode
+
+
+# the other workloads, each timed in the same run (the default workload is the
+# headline line); they are parity cases too
+OTHER_WORKLOADS = ("c2", "c3_t1", "c3_t32", "c3_t8192", "c4")
+
+
+def measure_other(moe, key, args, stream, flush, peaks, peak_src):
+    import torch
+    from synth import get_config
+    cfg = get_config(key)
+    layer = Layer(moe, cfg, args.seed, args.block_m, stream)
+    timed_loop(stream, flush, max(args.warmup, 3), layer.graph.replay)
+    times = timed_loop(stream, flush, args.workload_steps, layer.graph.replay)
+    st = layer.status()
+    if st != 0:
+        raise SystemExit(f"{key}: device status {moe.moe_status_string(st)}")
+    ms = statistics.median(times)
+    bd = breakdown(layer, flush, max(5, args.breakdown_iters // 2))
+    roof, layer_frac, ab, flops, decode = roofline_of(cfg, layer.routing_ids(), ms, bd, peaks, peak_src, key)
+    rec = {"workload": cfg.workload, "tokens_per_s": round(cfg.T / (ms / 1e3), 1), "ms_per_step": round(ms, 5),
+           "steps": len(times), "bound": roof["bound"], "layer_roofline_frac": round(layer_frac, 4),
+           "gemm1_frac": roof["frac"], "gemm1_ms": round(bd["gemm1_ms"], 5), "gemm2_ms": round(bd["gemm2_ms"], 5),
+           "breakdown_ms": {k2: round(v, 5) for k2, v in bd.items()},
+           "peak": roof["peak"], "peak_unit": roof["unit"], "active_experts": ab["active"],
+           "algorithmic_bytes": int(ab["total"]), "algorithmic_flops": int(flops),
+           "gpu_launches_per_step": layer.launches, "dtype": operand_dtype(cfg)}
+    del layer
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args):
     import torch
     import bit_block_scaled_gb300 as moe
     from bit_block_scaled_gb300 import build as _build
-    from synth import get_config, make_layer
+    from synth import get_config
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -215,46 +380,12 @@ def run_ours(args):
         pg.barrier()
     moe.load()
     cfg = get_config(args.config)
-    L = make_layer(cfg, seed=args.seed, device="cuda")
     T, E, k, H, I = cfg.T, cfg.E, cfg.k, cfg.H, cfg.I
     bm = args.block_m
-    nbytes = moe.moe_workspace_size(T, E, k, H, I, bm)
-    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
-    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    q13, q2 = moe.qweight(L["w13"]), moe.qweight(L["w2"])
-    act = moe.act(cfg.act, cfg.alpha, cfg.limit)
-    route = moe.ROUTE[cfg.route]
     stream = torch.cuda.Stream()
-
-    def fwd():
-        moe.moe_forward(L["x"], L["logits"], L["sel_bias"], k, route, q13, q2, 0, act, 1, bm, out, ws,
-                        stream)
-
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            fwd()
-    torch.cuda.synchronize()
-    launches_per_step = moe.moe_last_launch_count()
-    # capture one forward in a CUDA graph (the layer as a serving loop runs it)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            fwd()
-    torch.cuda.synchronize()
-    moe.moe_clear_status(ws, stream)
-
-    def timed_loop(n, run):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        with torch.cuda.stream(stream):
-            for i in range(n):
-                flush.zero_()               # evict L2 (untimed)
-                starts[i].record(stream)
-                run()
-                ends[i].record(stream)
-        torch.cuda.synchronize()
-        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    layer = Layer(moe, cfg, args.seed, bm, stream)
+    L = layer.L
 
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     bus = getattr(props, "pci_bus_id", None)
@@ -262,13 +393,13 @@ def run_ours(args):
                            f"{getattr(props, 'pci_device_id', 0):02x}.0" if bus is not None else local)
     sampler.start()
     time.sleep(0.3)
-    timed_loop(args.warmup, graph.replay)
+    timed_loop(stream, flush, args.warmup, layer.graph.replay)
     for attempt in range(2):
         if pg:
             pg.barrier()
         torch.cuda.synchronize()
         t0 = time.time()
-        times = timed_loop(args.steps, graph.replay)
+        times = timed_loop(stream, flush, args.steps, layer.graph.replay)
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
@@ -279,12 +410,12 @@ def run_ours(args):
             break
     sampler.stop()
     total_ms = sum(times)
-    st = moe.moe_read_status(ws, stream)
+    st = layer.status()
     if st != 0:
         raise SystemExit(f"device status {moe.moe_status_string(st)}")
 
-    # per-kernel breakdown: each step entry point timed with events on the stream
-    bd = breakdown(moe, L, cfg, bm, stream, flush, args.breakdown_iters)
+    # per-kernel breakdown: moe_forward_profile's events around each launch
+    bd = breakdown(layer, flush, args.breakdown_iters)
 
     # end to end through the C ABI with host buffers (pinned), copies inside
     xh = L["x"].cpu().pin_memory()
@@ -292,7 +423,8 @@ def run_ours(args):
     oh = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
 
     def e2e():
-        moe.moe_forward_host(xh, lh, L["sel_bias"], k, route, q13, q2, 0, act, 1, bm, oh, ws, stream)
+        moe.moe_forward_host(xh, lh, L["sel_bias"], k, layer.route, layer.q13, layer.q2, 0, layer.act, 1, bm, oh,
+                             layer.ws, stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -317,39 +449,10 @@ def run_ours(args):
     ms = total_ms / args.steps
     value = job_tokens_per_s(world, T, args.steps, total_ms)
     e2e_ms = e2e_total / len(e2e_times)
-    ids = None
-    try:
-        ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
-        tw = torch.empty(T, k, dtype=torch.float32, device="cuda")
-        moe.moe_route_topk(L["logits"], L["sel_bias"], k, route, ids, tw, ws, stream)
-        torch.cuda.synchronize()
-        ids = ids.cpu().numpy()
-    except Exception:
-        ids = None
-    ab = algorithmic_bytes(cfg, ids)
-    flops = algorithmic_flops(cfg)
     peaks, peak_src = read_peaks()
-    hbm = peaks["hbm_gbs"]
-    tc = peaks["bf16_tflops"]
-    gemm1_ms = bd["gemm1_ms"]
-    decode = flops / (tc * 1e12) < ab["total"] / (hbm * 1e9)
-    if decode:
-        g1_bytes = ab["w13"] + cfg.T * cfg.k * (cfg.H + cfg.I) * 2
-        achieved = g1_bytes / (gemm1_ms / 1e3) / 1e9
-        traffic, _ = read_traffic(f"gemm1_{args.config}")
-        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(achieved / hbm, 4), "traffic": traffic,
-                    "kernel": "grouped_gemm_kernel (GEMM1 + act)", "peak_source": peak_src,
-                    "algorithmic_bytes_per_launch": int(g1_bytes)}
-    else:
-        g1_flops = 2 * cfg.T * cfg.k * cfg.N1 * cfg.H
-        achieved = g1_flops / (gemm1_ms / 1e3) / 1e12
-        traffic, _ = read_traffic(f"gemm1_{args.config}")
-        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc, "unit": "TFLOP/s",
-                    "frac": round(achieved / tc, 4), "traffic": traffic,
-                    "kernel": "grouped_gemm_kernel (GEMM1 + act)", "peak_source": peak_src,
-                    "algorithmic_flops_per_launch": int(g1_flops)}
-    layer_frac = max(ab["total"] / (hbm * 1e9), flops / (tc * 1e12)) / (ms / 1e3)
+    roofline, layer_frac, ab, flops, _ = roofline_of(cfg, layer.routing_ids(), ms, bd, peaks, peak_src,
+                                                     args.config)
+    launches = layer.launches
     rec = {
         "metric": "MoE-layer tokens/s on 1 GB300; % of HBM BW (decode) / bf16 TC peak (prefill)",
         "value": round(value, 1),
@@ -362,11 +465,9 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": operand_dtype(cfg),
-        "data": "synthetic (seeded; weights N(0,0.02) quantised per the workload recipe)",
-        "config": {"workload": cfg.workload, "name": args.config, "T": T, "E": E, "top_k": k, "H": H,
-                   "I": I, "format": cfg.fmt, "activation": cfg.act, "block_m": bm,
-                   "parallelism": f"replicas x{world}", "l2": "flushed (256 MiB write) before every step",
-                   "launch": "CUDA graph of one moe_forward"},
+        "data": "synthetic (seeded CPU generators; weights N(0,0.02) quantised per the workload recipe)",
+        "config": workload_config(cfg, args, world),
+        "launch": "CUDA graph of one moe_forward per step",
         "layer_roofline_frac": round(layer_frac, 4),
         "algorithmic_bytes": int(ab["total"]),
         "algorithmic_flops": int(flops),
@@ -375,109 +476,138 @@ def run_ours(args):
         "e2e": {"value": round(job_tokens_per_s(world, T, 1, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": int(T * H * 2 + T * E * 4), "d2h_bytes_per_step": int(T * H * 2)},
-        "gpu_launches": int(launches_per_step * args.steps),
+        "gpu_launches": int(launches * args.steps),
         "clocks": clocks,
     }
+    del layer
+    torch.cuda.empty_cache()
+    if not args.no_workloads and world == 1:
+        rec["workloads"] = {key: measure_other(moe, key, args, stream, flush, peaks, peak_src)
+                            for key in OTHER_WORKLOADS if key != args.config}
     if not args.no_cpu_baseline and world == 1:
-        rec["cpu_baseline"] = cpu_baseline(cfg, L, args)
+        rec["cpu_baseline"] = cpu_baseline(cfg, args)
     print(json.dumps(rec), flush=True)
     if pg:
         pg.destroy_process_group()
 
 
-def breakdown(moe, L, cfg, bm, stream, flush, iters):
-    """Median device time of each of moe_forward's six kernels, as the forward
-    runs them (moe_forward_profile: CUDA events around each launch on the
-    stream; L2 flushed before each pass)."""
-    import torch
-    T, E, k, H, I = cfg.T, cfg.E, cfg.k, cfg.H, cfg.I
-    ws = torch.zeros(moe.moe_workspace_size(T, E, k, H, I, bm), dtype=torch.uint8, device="cuda")
-    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
-    act = moe.act(cfg.act, cfg.alpha, cfg.limit)
-    q13, q2 = moe.qweight(L["w13"]), moe.qweight(L["w2"])
-    route = moe.ROUTE[cfg.route]
-    res = {}
-    with torch.cuda.stream(stream):
-        for it in range(iters + 3):
-            flush.zero_()
-            ms = moe.moe_forward_profile(L["x"], L["logits"], L["sel_bias"], k, route, q13, q2, 0, act, 1, bm,
-                                         out, ws, stream)
-            if it >= 3:
-                for name, v in ms.items():
-                    res.setdefault(name, []).append(v)
-    med = {name: statistics.median(v) for name, v in res.items()}
-    return {"route_ms": med["route"], "align_gather_ms": med["align"] + med["gather"],
-            "gemm1_ms": med["gemm1"], "gemm2_ms": med["gemm2"], "unpermute_ms": med["unpermute"]}
-
-
 # ---------------------------------------------------------- the CPU oracle
-def oracle_step_sample(cfg, N, tokens):
-    """One oracle pass (routing, align, GEMMs, unpermute) over a token sample."""
+def oracle_batch(cfg, N, acc_dtype):
+    """One oracle pass (routing, align, GEMMs streamed per expert, unpermute)
+    over the whole batch of the workload."""
+    import numpy as np
     from oracle import layer as OL
     from oracle import routing as OR
-    sl = list(tokens)
-    return OL.moe_forward(N["x"][sl], N["logits"][sl], N["w13"], N["w2"], cfg.k,
+    return OL.moe_forward(N["x"], N["logits"], N["w13"], N["w2"], cfg.k,
                           route_mode=OR.ROUTE_TOPK_SOFTMAX if cfg.route == "topk_softmax"
                           else OR.ROUTE_SIGMOID_BIAS, sel_bias=N.get("sel_bias"),
                           act=OL.ACT_SWIGLUOAI if cfg.act == "swigluoai" else OL.ACT_RELU2,
-                          alpha=cfg.alpha, limit=cfg.limit)
+                          alpha=cfg.alpha, limit=cfg.limit, acc_dtype=np.dtype(acc_dtype))
 
 
-def cpu_baseline(cfg, L, args, budget_s=20.0):
+def oracle_layer_numpy(cfg, seed):
+    """Host NumPy copy of the workload, with only the routed experts' weights
+    drawn (the oracle never reads the others)."""
+    import numpy as np
+    from oracle import routing as OR
     from synth import to_numpy
-    N = to_numpy(L)
+    from synth.gen import make_activations, make_projection
+    d = make_activations(cfg, seed, "cpu")
+    logits = d["logits"].numpy()
+    if cfg.route == "topk_softmax":
+        ids, _ = OR.topk_softmax(logits, cfg.k)
+    else:
+        ids, _ = OR.sigmoid_bias_topk(logits, d["sel_bias"].numpy(), cfg.k)
+    experts = sorted(set(int(e) for e in np.unique(ids)))
+    d["w13"] = make_projection(cfg, "w13", cfg.N1, cfg.H, seed, "cpu", cfg.bias, experts=experts)
+    d["w2"] = make_projection(cfg, "w2", cfg.H, cfg.I, seed, "cpu", cfg.bias, experts=experts)
+    d["cfg"] = cfg
+    return to_numpy(d), len(experts)
+
+
+def oracle_child(args):
+    """Child process of the CPU baseline (BLAS threads fixed by its
+    environment): times one float32-accumulate oracle pass over the whole
+    batch of each named workload and prints one JSON object."""
+    from synth import get_config
+    res = {}
+    for key in args.oracle_child.split(","):
+        cfg = get_config(key)
+        N, active = oracle_layer_numpy(cfg, args.seed)
+        t0 = time.perf_counter()
+        oracle_batch(cfg, N, "float32")
+        el = time.perf_counter() - t0
+        res[key] = {"tokens_per_s": round(cfg.T / el, 4), "seconds": round(el, 3), "tokens": cfg.T,
+                    "active_experts": active}
+    print(json.dumps(res), flush=True)
+
+
+def _run_oracle_child(keys, threads, seed):
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", ",".join(keys),
+                        "--seed", str(seed)], env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise SystemExit("oracle child failed: " + r.stderr[-2000:])
+    return json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+
+
+def cpu_baseline(cfg, args):
+    """The oracle in float32-accumulate mode over the whole batch of the
+    workload (experts streamed one at a time), on all the host cores; plus
+    one-thread figures for the tiny layer, the decode layer and the
+    one-token MXFP4 layer."""
     cores = len(os.sched_getaffinity(0))
-    t0 = time.time()
-    done = 0
-    t = 0
-    while time.time() - t0 < budget_s and done < cfg.T:
-        oracle_step_sample(cfg, N, [t % cfg.T])
-        done += 1
-        t += 1
-    el = time.time() - t0
-    return {"value": round(done / el, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} token(s) of {args.config}, one oracle moe_forward per token "
-                      f"(float64 NumPy, full dequantisation of the routed experts each call)"}
+    main = _run_oracle_child([args.config], cores, args.seed)[args.config]
+    one = _run_oracle_child(["c0", "c1", "c3_t1"], 1, args.seed)
+    return {"value": main["tokens_per_s"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "mode": "float32 accumulate, whole batch, experts streamed one at a time",
+            "sample": f"one oracle pass over all {main['tokens']} tokens of {args.config} "
+                      f"({main['active_experts']} routed experts dequantised once each), "
+                      f"{main['seconds']} s, BLAS threads = {cores}",
+            "one_thread": {k2: v["tokens_per_s"] for k2, v in one.items()}}
 
 
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
         return
-    from synth import get_config, make_layer, to_numpy
+    import numpy as np
+    from synth import get_config
     cfg = get_config(args.config)
-    N = to_numpy(make_layer(cfg, seed=args.seed, device="cpu"))
+    N, active = oracle_layer_numpy(cfg, args.seed)
     cores = len(os.sched_getaffinity(0))
     budget = args.ref_budget_s
     t_start = time.time()
     for i in range(args.warmup):
-        oracle_step_sample(cfg, N, [i % cfg.T])
+        oracle_batch(cfg, N, np.float32)
         if time.time() - t_start > budget * 0.25:
             break
     times = []
     t0 = time.time()
     for i in range(args.steps):
-        s = time.time()
-        oracle_step_sample(cfg, N, [i % cfg.T])
-        times.append(time.time() - s)
+        s_ = time.perf_counter()
+        oracle_batch(cfg, N, np.float32)
+        times.append(time.perf_counter() - s_)
         if time.time() - t0 > budget:
             break
     total = sum(times)
-    value = len(times) / total
+    value = cfg.T * len(times) / total
     rec = {
         "metric": "MoE-layer tokens/s on 1 GB300; % of HBM BW (decode) / bf16 TC peak (prefill)",
         "impl": "reference",
         "value": round(value, 4), "unit": "tokens/s", "n_gpus": world, "steps": len(times),
         "steps_requested": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate (NumPy oracle)",
-        "data": "synthetic (seeded)",
-        "config": {"workload": cfg.workload, "name": args.config, "T": cfg.T, "E": cfg.E,
-                   "top_k": cfg.k, "H": cfg.H, "I": cfg.I, "format": cfg.fmt,
-                   "parallelism": "host cores, rank 0 only"},
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate (NumPy oracle)",
+        "data": "synthetic (seeded CPU generators)",
+        "config": workload_config(cfg, args, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "one token of the workload per step through the oracle's moe_forward; "
-                                   f"run capped at {budget:.0f} s"},
+                         "mode": "float32 accumulate, whole batch, experts streamed one at a time",
+                         "sample": f"each step one oracle pass over all {cfg.T} tokens of {args.config} "
+                                   f"({active} routed experts); run capped at {budget:.0f} s"},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -495,11 +625,16 @@ def main():
     ap.add_argument("--block-m", type=int, default=16)
     ap.add_argument("--breakdown-iters", type=int, default=20)
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--workload-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=150.0)
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    if args.impl == "reference":
+    if args.oracle_child:
+        oracle_child(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
