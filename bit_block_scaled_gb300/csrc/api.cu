@@ -232,9 +232,12 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
   return mark(6) ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// staging: the workspace must also hold moe_forward_host's staging buffers
+// for x, logits and out (they sit at its end); the device-pointer paths that
+// never touch them may pass false.
 static moe_status_t check_forward(const float *sel_bias, int T, int E, int k, int H, int I, int route,
                                   const moe_qweight_t *w13, const moe_qweight_t *w2, int layout, moe_act_t act,
-                                  int *block_m, void *ws, size_t ws_bytes, int mul) {
+                                  int *block_m, void *ws, size_t ws_bytes, int mul, bool staging = true) {
   if (*block_m == 0) *block_m = 16;
   if (mul < 0 || mul > 2) return MOE_ERR_INVALID_ARG;  // routing weight: none, on the output, on the input
   if (!valid_dims(T, E, k, H, I) || !valid_block_m(*block_m)) return MOE_ERR_INVALID_ARG;
@@ -247,9 +250,12 @@ static moe_status_t check_forward(const float *sel_bias, int T, int E, int k, in
   if ((s = check_weight(w13, E, N1, H)) != MOE_OK) return s;
   if ((s = check_weight(w2, E, H, I)) != MOE_OK) return s;
   if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < carve(T, E, k, H, I, *block_m).total) return MOE_ERR_WORKSPACE;
+  const Carve c = carve(T, E, k, H, I, *block_m);
+  if (ws_bytes < (staging ? c.total : c.xin)) return MOE_ERR_WORKSPACE;
   return MOE_OK;
 }
+
+
 
 moe_status_t moe_forward(const uint16_t *x, const float *logits, const float *sel_bias, int T, int E, int k, int H,
                          int I, int route, const moe_qweight_t *w13, const moe_qweight_t *w2, int gate_up_layout,
@@ -355,3 +361,35 @@ const char *moe_status_string(int status) {
 int moe_last_launch_count(void) { return g_last_launches; }
 
 }  // extern "C"
+
+namespace moe4 {
+
+// The fixed-workspace forward behind moe_forward_static: every host-side
+// check that moe_forward makes comes first (against the part of the
+// workspace the device-pointer path uses, without moe_forward_host's
+// staging buffers), so a rejected call enqueues nothing. Only then is the
+// status word cleared, the layer run and the status word copied out.
+moe_status_t forward_fixed_workspace(const uint16_t *x, const float *logits, const float *sel_bias, int T, int E,
+                                     int k, int H, int I, int route, const moe_qweight_t *w13,
+                                     const moe_qweight_t *w2, int layout, moe_act_t act, int mul, int block_m,
+                                     uint16_t *out, uint32_t *status_out, void *ws, size_t ws_bytes,
+                                     cudaStream_t st) {
+  g_last_launches = 0;
+  moe_status_t s = check_forward(sel_bias, T, E, k, H, I, route, w13, w2, layout, act, &block_m, ws, ws_bytes, mul,
+                                 /*staging=*/false);
+  if (s == MOE_ERR_WORKSPACE) return MOE_ERR_UNSUPPORTED;  // past the fixed workspace's capacity
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!aligned16(x) || !aligned16(logits) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (status_out && (reinterpret_cast<uintptr_t>(status_out) & 3u)) return MOE_ERR_INVALID_ARG;
+  // the workspace keeps the previous call's contents: only the status word
+  // has to start at zero (every intermediate is written before it is read)
+  if (cudaMemsetAsync(ws, 0, MOE_STATUS_BYTES, st) != cudaSuccess) return MOE_ERR_CUDA;
+  s = forward_impl(x, logits, sel_bias, T, E, k, H, I, route, w13, w2, layout, act, mul, block_m, out, ws, st);
+  if (s != MOE_OK) return s;
+  if (status_out && cudaMemcpyAsync(status_out, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace moe4

@@ -62,6 +62,15 @@ moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, co
                            const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches,
                            const float *tw = nullptr);
 
+// moe_forward with a fixed device workspace (moe_forward_static): all host
+// checks before anything is enqueued, then clear the status word, run the
+// layer and copy the status word to status_out (if not NULL).
+moe_status_t forward_fixed_workspace(const uint16_t *x, const float *logits, const float *sel_bias, int T, int E,
+                                     int k, int H, int I, int route, const moe_qweight_t *w13,
+                                     const moe_qweight_t *w2, int layout, moe_act_t act, int mul, int block_m,
+                                     uint16_t *out, uint32_t *status_out, void *ws, size_t ws_bytes,
+                                     cudaStream_t st);
+
 moe_status_t launch_unpermute(const uint16_t *y, const int32_t *row_pos, int T, int k, int H, int P_max,
                               uint16_t *out, unsigned int *status, cudaStream_t stream, int *launches);
 

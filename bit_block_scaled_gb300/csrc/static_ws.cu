@@ -9,18 +9,38 @@
 // library keeps that array until the process exits, and every call shares
 // it: calls whose work overlaps on the GPU (different streams, no ordering
 // between them) race on it and must not be issued.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_static_ws[MOE_STATIC_WS_BYTES];
 
 constexpr int kMaxDevices = 64;
-void *g_ws_ptr[kMaxDevices];
-cudaError_t g_ws_err[kMaxDevices];
-std::once_flag g_ws_once[kMaxDevices];
+std::atomic<void *> g_ws_ptr[kMaxDevices];  // set once a lookup on that device has succeeded
+std::mutex g_ws_mutex;
+
+// Device address of the array on the current device `dev`. In host code the
+// array's name is only a host-side stand-in, so its address is looked up with
+// that device current. Only a successful lookup is kept; a failed one (for
+// example made during a stream capture) is retried by the next call.
+void *static_ws_address(int dev) {
+  void *p = g_ws_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  p = g_ws_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) {
+      (void)cudaGetLastError();  // the failed lookup leaves no error behind for the next CUDA call
+      return nullptr;
+    }
+    g_ws_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
 
 }  // namespace
 
@@ -31,25 +51,11 @@ extern "C" moe_status_t moe_forward_static(const uint16_t *x, const float *logit
                                            uint32_t *status_out, moe_stream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-  // Once per device, with that device current: the device address of the
-  // array (in host code its name is only a host-side stand-in).
-  std::call_once(g_ws_once[dev], [dev] {
-    g_ws_err[dev] = cudaGetSymbolAddress(&g_ws_ptr[dev], g_static_ws);
-  });
-  if (g_ws_err[dev] != cudaSuccess || g_ws_ptr[dev] == nullptr) return MOE_ERR_CUDA;
-  size_t need = 0;
-  moe_status_t s = moe_workspace_size(T, E, k, H, I, block_m, &need);
-  if (s != MOE_OK) return s;
-  if (need > MOE_STATIC_WS_BYTES) return MOE_ERR_UNSUPPORTED;  // sizes past the array's capacity
-  cudaStream_t st = (cudaStream_t)stream;
-  // the array keeps the previous call's contents: only the status word has
-  // to start at zero (every intermediate is written before it is read)
-  if (cudaMemsetAsync(g_ws_ptr[dev], 0, MOE_STATUS_BYTES, st) != cudaSuccess) return MOE_ERR_CUDA;
-  s = moe_forward(x, logits, sel_bias, T, E, k, H, I, route, w13, w2, gate_up_layout, act, mul_topk_weights,
-                  block_m, out, g_ws_ptr[dev], MOE_STATIC_WS_BYTES, stream);
-  if (s != MOE_OK) return s;
-  if (status_out &&
-      cudaMemcpyAsync(status_out, g_ws_ptr[dev], sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  void *ws = static_ws_address(dev);
+  if (!ws) return MOE_ERR_CUDA;
+  // every argument is checked before anything is enqueued; sizes past the
+  // array's capacity return MOE_ERR_UNSUPPORTED
+  return moe4::forward_fixed_workspace(x, logits, sel_bias, T, E, k, H, I, route, w13, w2, gate_up_layout, act,
+                                       mul_topk_weights, block_m, out, status_out, ws, MOE_STATIC_WS_BYTES,
+                                       (cudaStream_t)stream);
 }

@@ -249,14 +249,20 @@ moe_status_t moe_forward_profile(const uint16_t *x, const float *logits,
  * counterpart on the source pages; it is a deployment convenience.
  * The workspace is a file-scope device array of MOE_STATIC_WS_BYTES inside
  * the library; every GPU that loads the library holds it until the process
- * exits. Sizes whose moe_workspace_size exceeds it return
- * MOE_ERR_UNSUPPORTED before anything is launched (at H = I = 2880, E = 32
- * that is about 1,900 routed rows T*k).
+ * exits. The call needs moe_workspace_size's bytes minus the staging buffers
+ * of moe_forward_host (which it never uses); sizes past the array return
+ * MOE_ERR_UNSUPPORTED (at H = I = 2880, E = 32, top-4, block_m 16 the
+ * array holds up to T = 607 tokens, 2,428 routed rows).
+ * Every argument is checked before anything is enqueued: a call that returns
+ * MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED leaves the stream, the array and
+ * status_out untouched, and so does a call with T = 0.
  * The first call on a device looks up the array's device address, so make it
- * before any stream capture. All calls share the array: calls that overlap on
- * the GPU race and must not be issued. Each call clears the array's status
- * word first; status_out (device, may be NULL) receives the raw status word
- * after the call (bit c-1 set when device error code c was detected).
+ * before any stream capture; if that lookup fails the call returns
+ * MOE_ERR_CUDA and the next call tries again. All calls share the array:
+ * calls that overlap on the GPU race and must not be issued. Each call clears
+ * the array's status word first; status_out (device, 4-byte aligned, may be
+ * NULL) receives the raw status word after the call (bit c-1 set when device
+ * error code c was detected).
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 #define MOE_STATIC_WS_BYTES (32u << 20)
 moe_status_t moe_forward_static(const uint16_t *x, const float *logits,
