@@ -181,7 +181,8 @@ def swigluoai(gate: np.ndarray, up: np.ndarray, alpha: float, limit: float) -> n
     u = np.clip(up.astype(np.float64), -np.float64(np.float32(limit)),
                 np.float64(np.float32(limit)))
     a = np.float64(np.float32(alpha))
-    return f32((u + 1.0) * g * (1.0 / (1.0 + np.exp(-a * g))))
+    with np.errstate(over="ignore"):  # exp overflow gives sigmoid 0, the exact limit
+        return f32((u + 1.0) * g * (1.0 / (1.0 + np.exp(-a * g))))
 
 
 def relu2(h: np.ndarray) -> np.ndarray:
