@@ -12,10 +12,16 @@
 // The kernel is persistent, one CTA per SM (it takes all 512 TMEM columns):
 // each CTA walks the tiles blockIdx.x, blockIdx.x + gridDim.x, ... and every
 // role derives the tile coordinates by itself from expert_offsets, so roles
-// synchronise on data only. Warp roles (832 threads):
+// synchronise on data only. Warp roles (864 threads):
 //   warp 0        TMA producer: per tile the block scales (bulk copy, two
-//                 buffers), then per stage the packed 4-bit weight rows and
-//                 the token rows; it runs ahead into the next tile
+//                 buffers), then per stage the packed 4-bit weight rows (and,
+//                 for wide token tiles, the token rows in the same ring slot);
+//                 it runs ahead into the next tile
+//   warp 26       narrow token tiles (decode, four K blocks per stage): the
+//                 token rows, in a ring of their own. The weight slot is then
+//                 released as soon as the dequantisation warps have read it,
+//                 not when the MMAs that read the token rows complete, so
+//                 more weight bytes stay in flight
 //   warp 1        TMEM allocation; one lane issues tcgen05.mma (kind::f16, A
 //                 from TMEM, B from shared memory) into one of two TMEM
 //                 accumulators
@@ -57,7 +63,8 @@ namespace {
 
 constexpr int kFirstDqWarp = 2, kDqWarps = 16;
 constexpr int kFirstEpiWarp = kFirstDqWarp + kDqWarps, kEpiWarps = 8;
-constexpr int kWarps = kFirstEpiWarp + kEpiWarps;
+constexpr int kXWarp = kFirstEpiWarp + kEpiWarps;  // token-row producer of the split rings
+constexpr int kWarps = kXWarp + 1;
 constexpr int kThreads = kWarps * 32;
 constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kDqGroupThreads = kDqThreads / 2;  // one of the two dequant groups
@@ -82,10 +89,10 @@ __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v
 
 // Shared-memory carve-up; identical on host (sizing) and device (addresses).
 __host__ __device__ inline Smem smem_layout(int tile_n, int stages, int kpb, int sc_row_bytes,
-                                            int z_row_bytes) {
+                                            int z_row_bytes, int xstages) {
   Smem s;
   uint32_t o = 0;
-  s.x = o;    o += stages * kpb * tile_n * 128;
+  s.x = o;    o += xstages * kpb * tile_n * 128;
   o = align_up(o, 1024);
   s.w = o;    o += stages * kTileM * 32 * kpb;
   s.sc = o;   o += 2 * align_up(kTileM * sc_row_bytes, 128);
@@ -97,7 +104,7 @@ __host__ __device__ inline Smem smem_layout(int tile_n, int stages, int kpb, int
   s.tw = o;   o += kEpiWarps * tile_n * 4;
   s.ex = o;   o += kEpiWarps * tile_n * 4;
   o = align_up(o, 8);
-  s.bar = o;  o += (2 * kMaxStagesL + 2 * kMaxNA + 8) * 8;
+  s.bar = o;  o += (4 * kMaxStagesL + 2 * kMaxNA + 8) * 8;
   s.misc = o; o += 64;
   s.total = o + 1024;  // slack for aligning the dynamic base to 1024
   return s;
@@ -176,7 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   // 1024-byte aligned start (pointer arithmetic on the shared array keeps the
   // compiler's knowledge that all these addresses are shared memory)
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const Smem L = smem_layout(p.tile_n, p.stages, KPB, p.sc_row_bytes, p.z_row_bytes);
+  // narrow token tiles: weights and token rows in separate rings (warp 26
+  // loads the token rows; a weight slot is freed once it has been dequantised)
+  constexpr bool SPLIT = KPB == 4;
+  const int NX = SPLIT ? p.xstages : p.stages;
+  const Smem L = smem_layout(p.tile_n, p.stages, KPB, p.sc_row_bytes, p.z_row_bytes, NX);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NA = p.na;                     // operand buffers in TMEM
   constexpr int kpb = KPB;                 // K blocks per pipeline stage
@@ -192,6 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   auto scempty_bar = [&](int s) { return bar0 + 8u * (kB3 + 2 + s); };
   auto accfull_bar = [&](int s) { return bar0 + 8u * (kB3 + 4 + s); };
   auto accempty_bar = [&](int s) { return bar0 + 8u * (kB3 + 6 + s); };
+  constexpr int kB4 = kB3 + 8;
+  auto xfull_bar = [&](int s) { return bar0 + 8u * (kB4 + s); };
+  auto wempty_bar = [&](int s) { return bar0 + 8u * (kB4 + kMaxStagesL + s); };
   volatile int *misc = reinterpret_cast<volatile int *>(base + L.misc);  // [0] tmem, [1] abort
   int *offs_s = reinterpret_cast<int *>(base + L.offs);
   int *ids_s = reinterpret_cast<int *>(base + L.ids);
@@ -209,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(done_bar(s), 1);
+      mbar_init(wempty_bar(s), kDqGroupThreads / 32);
+      mbar_init(xfull_bar(s), 1);
     }
     for (int s = 0; s < NA; ++s) {
       mbar_init(dq_bar(s), kDqGroupThreads);
@@ -308,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       }
       rsc.advance(2);
       for (int st = 0; st < NS; ++st) {
-        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(done_bar(rst.slot), rst.phase ^ 1);
+        ok = !((issued_mask >> rst.slot) & 1u) ||
+             mbar_wait(SPLIT ? wempty_bar(rst.slot) : done_bar(rst.slot), rst.phase ^ 1);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -318,15 +335,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const int kb0 = st * kpb;
           const int nkb = min(kpb, KB - kb0);
           const uint32_t fb = full_bar(rst.slot);
-          mbar_arrive_expect_tx(fb, (64 + rows1) * rb + (uint32_t)(nkb * p.tile_n * 128));
+          mbar_arrive_expect_tx(fb, (64 + rows1) * rb + (SPLIT ? 0u : (uint32_t)(nkb * p.tile_n * 128)));
           const uint32_t ws = w_s + rst.slot * (kTileM * rb);
           tma_load_3d(ws, &p.tm_w, fb, st * (int)rb, wrow0, tt.e);
           if (rows1) tma_load_3d(ws + 64 * rb, &p.tm_w, fb, st * (int)rb, wrow1, tt.e);
           const uint32_t xs0 = x_s + rst.slot * xstage;
           // one box of tile_n token rows per K block (rows past the tile's
           // own are loaded but never read by the MMA)
-          for (int j = 0; j < nkb; ++j)
-            tma_load_2d(xs0 + j * (p.tile_n * 128), &p.tm_x, fb, (kb0 + j) * kBK, tt.row0);
+          if (!SPLIT)
+            for (int j = 0; j < nkb; ++j)
+              tma_load_2d(xs0 + j * (p.tile_n * 128), &p.tm_x, fb, (kb0 + j) * kBK, tt.row0);
         }
         issued_mask |= 1u << rst.slot;
         issued_par = (issued_par & ~(1u << rst.slot)) | ((uint32_t)rst.phase << rst.slot);
@@ -360,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       for (int st = 0; st < NS; ++st) {
         const int kb0 = st * kpb;
         const int nkb = min(kpb, KB - kb0);
-        ok = mbar_wait(full_bar(rs.slot), rs.phase) && mbar_wait(dq_bar(ra.slot), ra.phase);
+        ok = mbar_wait(SPLIT ? xfull_bar(rs.slot) : full_bar(rs.slot), rs.phase) && mbar_wait(dq_bar(ra.slot), ra.phase);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -386,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         __syncwarp();
         ra.advance(NA);
-        rs.advance(p.stages);
+        rs.advance(NX);
       }
       if (!ok) break;
       const uint32_t ab = accfull_bar(rc.slot);
@@ -439,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if ((kdone & 1) != grp) {  // the other group's stage
           ca.advance(NA);
           cs.advance(p.stages);
-          if (kdone >= NA) cl.advance(p.stages);
+          if (kdone >= NA) cl.advance(NX);
           continue;
         }
         const int kb0 = st * kpb;
@@ -454,6 +472,46 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           break;
         }
         tc_fence_after();
+        if (F16) {
+          // f16 operands (NVFP4, MXFP4): hardware E2M1 -> f16 pairs in natural
+          // K order, times the block scale as f16 (NVFP4: the E4M3 value;
+          // MXFP4: 2^(e8 - 115)). All of this warp's shared-memory loads for
+          // the stage are issued first, then the arithmetic and TMEM stores.
+          uint4 cw[nw];
+          uint32_t sv[nw][2];
+#pragma unroll
+          for (int i = 0; i < nw; ++i) {
+            const int ch = kq * nw + i;
+            const int j = ch >> 1, hk = ch & 1;
+            const int kb = min(kb0 + j, KB - 1);
+            cw[i] = *reinterpret_cast<const uint4 *>(w_row + cs.slot * (kTileM * rb) + ((ch ^ sw) << 4));
+            if (FMT == MOE_FMT_NVFP4) {
+              const uint32_t sb = *reinterpret_cast<const uint16_t *>(sc_row + kb * 4 + hk * 2);
+              sv[i][0] = lut[sb & 0xFFu];
+              sv[i][1] = lut[(sb >> 8) & 0xFFu];
+            } else {
+              const uint32_t e8 = sc_row[kb * 2 + hk];
+              if (row_ok && j < nkb && e8 > 128u && e8 != 255u) raise_status(p.status, MOE_ERR_SCALE_RANGE);
+              sv[i][0] = sv[i][1] = lut[e8];
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < nw; ++i) {
+            const int ch = kq * nw + i;
+            const int j = ch >> 1, hk = ch & 1;
+            uint32_t out[16];
+            const uint32_t xw[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+#pragma unroll
+              for (int b = 0; b < 4; ++b) out[h * 4 + b] = hmul2(e2m1x2_f16x2(xw[h], b), sv[i][h >> 1]);
+            if (!row_ok) {
+#pragma unroll
+              for (int q = 0; q < 16; ++q) out[q] = 0u;
+            }
+            if (j < nkb) tmem_st16(t_a + (32u * kpb) * ca.slot + 32u * j + 16u * hk, out);
+          }
+        } else
 #pragma unroll
         for (int i = 0; i < nw; ++i) {
           const int ch = kq * nw + i;  // 16-byte chunk of the row: K block ch / 2, half ch % 2
@@ -465,18 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
               const uint4 c = *reinterpret_cast<const uint4 *>(w_row + cs.slot * (kTileM * rb) +
                                                               ((ch ^ sw) << 4));
               const uint32_t xw[4] = {c.x, c.y, c.z, c.w};
-              if (FMT == MOE_FMT_NVFP4 && F16) {
-                // hardware E2M1 -> f16 pairs (natural K order), times the f16 scale
-                const uint32_t sb = *reinterpret_cast<const uint16_t *>(sc_row + kb * 4 + hk * 2);
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                  const uint32_t s2 = lut[(sb >> (8 * g)) & 0xFFu];
-#pragma unroll
-                  for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) out[(2 * g + h) * 4 + b] = hmul2(e2m1x2_f16x2(xw[2 * g + h], b), s2);
-                }
-              } else if (FMT == MOE_FMT_NVFP4) {
+              if (FMT == MOE_FMT_NVFP4) {
                 const uint32_t sb = *reinterpret_cast<const uint16_t *>(sc_row + kb * 4 + hk * 2);
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
@@ -493,19 +540,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint32_t e8 = sc_row[kb * 2 + hk];
                 if (e8 > 128u && e8 != 255u) raise_status(p.status, MOE_ERR_SCALE_RANGE);
                 const uint32_t s2 = lut[e8];
-                if (F16) {  // hardware E2M1 -> f16 pairs (natural K order) times 2^(e8 - 115)
 #pragma unroll
-                  for (int h = 0; h < 4; ++h)
+                for (int h = 0; h < 4; ++h) {
+                  uint32_t o4[4];
+                  e2m1x8_raw(xw[h], o4);
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) out[h * 4 + b] = hmul2(e2m1x2_f16x2(xw[h], b), s2);
-                } else {
-#pragma unroll
-                  for (int h = 0; h < 4; ++h) {
-                    uint32_t o4[4];
-                    e2m1x8_raw(xw[h], o4);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) out[h * 4 + q] = bmul2(o4[q], s2);
-                  }
+                  for (int q = 0; q < 4; ++q) out[h * 4 + q] = bmul2(o4[q], s2);
                 }
               } else {  // INT4, one group of 64 per K block
                 // bf16_rne((q - z) * s) with a single rounding, on bf16 pairs:
@@ -537,16 +577,57 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             tmem_st16(t_a + (32u * kpb) * ca.slot + 32u * j + 16u * hk, out);
           }
         }
+        if (SPLIT) {  // this warp has read its rows of the weight slot
+          __syncwarp();
+          if (lane == 0) mbar_arrive(wempty_bar(cs.slot));
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(dq_bar(ca.slot));
         ca.advance(NA);
         cs.advance(p.stages);
-        if (kdone >= NA) cl.advance(p.stages);
+        if (kdone >= NA) cl.advance(NX);
       }
       if (!ok) break;
       mbar_arrive(scempty_bar(rsc.slot));  // done with this tile's scales
       rsc.advance(2);
+    }
+  } else if (warp == kXWarp) {
+    // ============================================================ token rows (split rings)
+    if (SPLIT) {
+      const bool leader = lane == 0;
+      if (leader) prefetch_tmap(&p.tm_x);
+      const uint32_t x_s = smem_u32(base + L.x);
+      const uint32_t xstage = (uint32_t)kpb * p.tile_n * 128;
+      Ring rx;
+      uint32_t issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
+        for (int st = 0; st < NS; ++st) {
+          ok = !((issued_mask >> rx.slot) & 1u) || mbar_wait(done_bar(rx.slot), rx.phase ^ 1);
+          ok = __all_sync(0xffffffffu, ok && !misc[1]);
+          if (!ok) {
+            fail(leader);
+            break;
+          }
+          if (leader) {
+            const int kb0 = st * kpb;
+            const int nkb = min(kpb, KB - kb0);
+            const uint32_t fb = xfull_bar(rx.slot);
+            mbar_arrive_expect_tx(fb, (uint32_t)(nkb * p.tile_n * 128));
+            const uint32_t xs0 = x_s + rx.slot * xstage;
+            for (int j = 0; j < nkb; ++j)
+              tma_load_2d(xs0 + j * (p.tile_n * 128), &p.tm_x, fb, (kb0 + j) * kBK, tt.row0);
+          }
+          issued_mask |= 1u << rx.slot;
+          issued_par = (issued_par & ~(1u << rx.slot)) | ((uint32_t)rx.phase << rx.slot);
+          rx.advance(NX);
+        }
+      }
+      if (!ok && leader)
+        for (int q = 0; q < NX; ++q)
+          if ((issued_mask >> q) & 1u) (void)mbar_wait(xfull_bar(q), (issued_par >> q) & 1u);
     }
   } else {
     // ============================================================ epilogue
@@ -816,12 +897,16 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   // stages: as many as fit in shared memory
   const uint32_t budget = 225 * 1024;
   int stages = kMaxStagesL;
-  while (stages > 2 && smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes).total > budget) --stages;
+  const bool split = kpb == 4;
+  const int xst = split ? 4 : 0;
+  a.xstages = xst;
+  while (stages > 2 && smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes, split ? xst : stages).total > budget) --stages;
   a.stages = stages;
+  if (split && a.na > xst) a.na = xst;
   // an operand buffer is freed by the done barrier of its previous stage's
   // ring slot, which must not have been reused meanwhile: NA <= stages
   if (a.na > stages) a.na = stages;
-  uint32_t smem = smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes).total;
+  uint32_t smem = smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes, split ? xst : stages).total;
   // one CTA per SM: it allocates all of TMEM
   if (smem < 120 * 1024) smem = 120 * 1024;
   if (smem > kMaxSmem) return MOE_ERR_UNSUPPORTED;

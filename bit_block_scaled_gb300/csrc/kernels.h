@@ -24,7 +24,7 @@ struct GemmArgs {
   unsigned int *status;
   int E, N, K, P_max, num_rows, ldo, layout, I, mul, a_f16;
   float alpha, limit;
-  int tile_n, stages, kpb, sc_row_bytes, z_row_bytes, m_tiles, nacc, na;
+  int tile_n, stages, kpb, sc_row_bytes, z_row_bytes, m_tiles, nacc, na, xstages;
 };
 
 int choose_tile_n(int num_rows, int E);
