@@ -638,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
     int *ids_w = ids_s + (warp - kFirstEpiWarp) * p.tile_n;  // this warp's copy of the row ids
     float *tw_w = tw_s + (warp - kFirstEpiWarp) * p.tile_n;
-    int *ex_w = reinterpret_cast<int *>(base + L.ex) + (warp - kFirstEpiWarp) * p.tile_n;
+    // per-token 2^e of the f16 activation rows (GEMM1; else 1)
+    float *gm_w = reinterpret_cast<float *>(base + L.ex) + (warp - kFirstEpiWarp) * p.tile_n;
     Ring rc;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -646,7 +647,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
       const int e = tt.e, row0 = tt.row0, nrows = tt.nrows;
       const int n16 = (nrows + 15) & ~15;
-      // this tile's row ids and routing weights, staged per warp
+      float gmul = 1.f;
+      // undo the operands' power-of-two folds: bf16 NVFP4 weights carry 2^-8,
+      // f16 MXFP4 weights 2^12, and a f16 GEMM2 reads a scaled by 2^9
+      const float afold = (F16 && EPI == EPI_WEIGHTED) ? 0x1p-9f : 1.f;
+      if (FMT == MOE_FMT_NVFP4) gmul = F16 ? p.gscale[e] * afold : p.gscale[e] * 256.f;
+      if (FMT == MOE_FMT_MXFP4 && F16) gmul = 0x1p-12f * afold;
+      // this tile's row ids, routing weights and multipliers, staged per warp
       __syncwarp();
       for (int i = lane; i < n16; i += 32) {
         int sid = p.num_rows;
@@ -655,7 +662,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         float w = 0.f;
         if (EPI == EPI_WEIGHTED && p.mul && sid >= 0 && sid < p.num_rows) w = p.topk_w[sid];
         tw_w[i] = w;
-        if (F16 && EPI != EPI_WEIGHTED) ex_w[i] = (i < nrows) ? p.xexp[row0 + i] : 0;
+        float gm = 1.f;  // undoes the activation row's 2^-e (exact)
+        if (F16 && EPI != EPI_WEIGHTED && i < nrows) gm = __uint_as_float((uint32_t)(127 + p.xexp[row0 + i]) << 23);
+        gm_w[i] = gm;
       }
       __syncwarp();
       int n_w, col;
@@ -672,12 +681,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       // GEMM1 writes its output interleaved within groups of 8 columns (the
       // layout GEMM2 reads its activations in): column c sits at 2*(c%4)+c/4
       const int col_st = (col & ~7) | ((col & 3) << 1) | ((col >> 2) & 1);
-      float gmul = 1.f;
-      // undo the operands' power-of-two folds: bf16 NVFP4 weights carry 2^-8,
-      // f16 MXFP4 weights 2^12, and a f16 GEMM2 reads a scaled by 2^9
-      const float afold = (F16 && EPI == EPI_WEIGHTED) ? 0x1p-9f : 1.f;
-      if (FMT == MOE_FMT_NVFP4) gmul = F16 ? p.gscale[e] * afold : p.gscale[e] * 256.f;
-      if (FMT == MOE_FMT_MXFP4 && F16) gmul = 0x1p-12f * afold;
       float bias = 0.f;
       if (p.bias && col_ok) bias = bf16_bits_to_float(p.bias[(size_t)e * p.N + n_w]);
       bool lok = true;
@@ -692,38 +695,63 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       for (int c0 = 16 * eh; c0 < n16; c0 += 32) {
         uint32_t v[16];
         tmem_ld16(ta + c0, v);
+        // which of these 16 tokens are stored (one shared-memory read per lane)
+        const int ltok = c0 + (lane & 15);
+        const int lsid = ids_w[ltok];
+        const uint32_t smask =
+            col_ok ? (__ballot_sync(0xffffffffu, ltok < nrows && lsid >= 0 && lsid < p.num_rows) & 0xFFFFu) : 0u;
+        float gm[16];
+        if (F16 && EPI != EPI_WEIGHTED) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 g4 = *reinterpret_cast<const float4 *>(gm_w + c0 + 4 * q);
+            gm[4 * q] = g4.x;
+            gm[4 * q + 1] = g4.y;
+            gm[4 * q + 2] = g4.z;
+            gm[4 * q + 3] = g4.w;
+          }
+        }
         tmem_ld_wait();
+        float h[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int tok = c0 + j;
-          const int sid = ids_w[tok];
-          const bool store = tok < nrows && sid >= 0 && sid < p.num_rows && col_ok;
           float acc = __uint_as_float(v[j]);
-          if (F16 && EPI != EPI_WEIGHTED)  // undo the activation row's 2^-e (exact)
-            acc = __fmul_rn(acc, __uint_as_float((uint32_t)(127 + ex_w[tok]) << 23));
-          float h = __fadd_rn(__fmul_rn(acc, gmul), bias);
-          uint16_t *orow = p.out + (size_t)(row0 + tok) * p.ldo;
-          if (EPI == EPI_SWIGLU) {
-            const float other = __shfl_xor_sync(0xffffffffu, h, 1);
-            if (!(r & 1) && store) {
-              const float g = fminf(h, p.limit);
-              const float u = fminf(fmaxf(other, -p.limit), p.limit);
+          if (F16 && EPI != EPI_WEIGHTED) acc = __fmul_rn(acc, gm[j]);
+          h[j] = __fadd_rn(__fmul_rn(acc, gmul), bias);
+        }
+        if (EPI == EPI_SWIGLU) {
+          // gate and up rows are adjacent lanes: the even lane finishes tokens
+          // 0..7 of the chunk and the odd lane tokens 8..15, each after one
+          // exchange per token pair, so no lane idles
+          const bool odd = r & 1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? h[j] : h[8 + j], 1);
+            const int jt = odd ? 8 + j : j;
+            if ((smask >> jt) & 1u) {
+              const float g = fminf(odd ? recv : h[j], p.limit);
+              const float u = fminf(fmaxf(odd ? h[8 + j] : recv, -p.limit), p.limit);
               const float sg = __fdividef(1.0f, 1.0f + __expf(-p.alpha * g));  // fast-math sigmoid
               const uint16_t ab = float_to_bf16_bits((u + 1.0f) * g * sg);  // R1
+              uint16_t *orow = p.out + (size_t)(row0 + c0 + jt) * p.ldo;
               if (F16 && p.a_f16)  // the bf16 value times 2^9, held as f16 for an f16 GEMM2, natural order
                 orow[col] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(ab) * 512.f));
               else
                 orow[col_st] = ab;
             }
-          } else if (EPI == EPI_RELU2) {
-            if (store) {
-              const float rr = fmaxf(h, 0.f);
-              orow[col_st] = float_to_bf16_bits(rr * rr);
-            }
-          } else {
-            if (store) {
-              if (p.mul) h = __fmul_rn(h, tw_w[tok]);
-              orow[col] = float_to_bf16_bits(h);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if ((smask >> j) & 1u) {
+              uint16_t *orow = p.out + (size_t)(row0 + c0 + j) * p.ldo;
+              if (EPI == EPI_RELU2) {
+                const float rr = fmaxf(h[j], 0.f);
+                orow[col_st] = float_to_bf16_bits(rr * rr);
+              } else {
+                const float hw = p.mul ? __fmul_rn(h[j], tw_w[c0 + j]) : h[j];
+                orow[col] = float_to_bf16_bits(hw);
+              }
             }
           }
         }
