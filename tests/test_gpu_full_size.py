@@ -197,7 +197,9 @@ def test_full_size_workload(key, n_sample):
         checked += len(slots)
     assert len(picked) == len({int(e) for e in ids.reshape(-1)})   # every active expert
     out_g = _host(out[tokens])
+    steps_g = _host(g["out"][tokens])
     for n, t in enumerate(tokens):
         y_tok = np.stack([y_ref_of[int(row_pos[t * k + j])] for j in range(k)])
         o_ref = OL.unpermute_reduce(y_tok, np.arange(k), 1, k)[0]
-        assert_close(out_g[n], o_ref, f"{key} out, token {t}")
+        assert_close(out_g[n], o_ref, f"{key} out (moe_forward), token {t}")
+        assert_close(steps_g[n], o_ref, f"{key} out (steps), token {t}")
