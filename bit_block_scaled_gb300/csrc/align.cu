@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kAlignThreads = 1024;
 constexpr int kMaxE = 256;
+constexpr int kAlignSplitRows = 4096;  // from this many routed rows on, the alignment runs over many CTAs
 
 __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__restrict__ ids, int R, int E,
                                                               int bm, int P_max, int32_t *__restrict__ sorted,
@@ -138,6 +139,133 @@ __device__ __forceinline__ uint4 weigh8(uint4 q, float w) {
   return make_uint4(weigh_bf16x2(q.x, w), weigh_bf16x2(q.y, w), weigh_bf16x2(q.z, w), weigh_bf16x2(q.w, w));
 }
 
+// The same alignment for large batches, over many CTAs: the rows are cut into
+// chunks of kChunkRows in row order. align_count_kernel counts each chunk's
+// rows per expert; align_place_kernel then lets every CTA derive, from all the
+// chunks' counts, the padded expert offsets and the first slot of its own
+// chunk in each expert (the slots of the earlier chunks' rows come first), and
+// place its rows exactly as the one-CTA kernel would: ascending flat row id
+// within each expert, so the result is the same bytes.
+constexpr int kChunkRows = kAlignThreads;  // one row per thread
+
+__global__ void __launch_bounds__(kAlignThreads) align_count_kernel(const int32_t *__restrict__ ids, int R, int E,
+                                                                    int32_t *__restrict__ counts,
+                                                                    int32_t *__restrict__ row_pos,
+                                                                    unsigned int *status) {
+  __shared__ int cnt[kMaxE];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += kAlignThreads) cnt[e] = 0;
+  __syncthreads();
+  const int r = blockIdx.x * kChunkRows + tid;
+  if (r < R) {
+    const int e = ids[r];
+    if (e < 0 || e >= E) {
+      raise_status(status, MOE_ERR_BAD_INDEX);
+      row_pos[r] = -1;
+    } else {
+      atomicAdd(&cnt[e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kAlignThreads) counts[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_place_kernel(const int32_t *__restrict__ ids, int R, int E,
+                                                                    int bm, int P_max, int nchunks,
+                                                                    const int32_t *__restrict__ counts,
+                                                                    int32_t *__restrict__ sorted,
+                                                                    int32_t *__restrict__ offsets,
+                                                                    int32_t *__restrict__ block_ids,
+                                                                    int32_t *__restrict__ row_pos) {
+  __shared__ int off[kMaxE + 1];
+  __shared__ int tot[kMaxE];
+  __shared__ int bef[kMaxE];        // rows of the earlier chunks, per expert
+  __shared__ int wcnt[32 * kMaxE];  // [warp][expert]: counts, then first slot
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x;
+  // each expert's total and the rows of the chunks before this one
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int t = 0, before = 0;
+    for (int q = 0; q < nchunks; ++q) {
+      const int v = counts[(size_t)q * E + e];
+      if (q < c) before += v;
+      t += v;
+    }
+    tot[e] = t;
+    bef[e] = before;
+  }
+  __syncthreads();
+  if (warp == 0) {  // padded offsets
+    int running = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int pc = e < E ? (tot[e] + bm - 1) / bm * bm : 0;
+      int incl = pc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) off[e] = running + incl - pc;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) off[E] = running;
+  }
+  // per-warp counts of this chunk, in row order
+  const int r = c * kChunkRows + tid;
+  int e_r = -1;
+  if (r < R) {
+    e_r = ids[r];
+    if (e_r < 0 || e_r >= E) e_r = -1;
+  }
+  for (int e = lane; e < E; e += 32) wcnt[warp * E + e] = 0;
+  __syncwarp();
+  const unsigned peers = __match_any_sync(0xffffffffu, e_r);
+  if (e_r >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e_r] = __popc(peers);
+  __syncthreads();
+  // first slot of each warp's rows in each expert
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int run = off[e] + bef[e];
+    for (int w = 0; w < 32; ++w) {
+      const int cw = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += cw;
+    }
+  }
+  __syncthreads();
+  if (e_r >= 0) {
+    const int pos = wcnt[warp * E + e_r] + __popc(peers & ((1u << lane) - 1u));
+    sorted[pos] = r;
+    row_pos[r] = pos;
+  }
+  // padding slots of this CTA's share of the experts, the slots past the
+  // last expert, the block -> expert table and the offsets
+  for (int e = c; e < E; e += gridDim.x)
+    for (int q = off[e] + tot[e] + tid; q < off[e + 1]; q += kAlignThreads) sorted[q] = R;
+  if (c == 0) {
+    for (int q = off[E] + tid; q < P_max; q += kAlignThreads) sorted[q] = R;
+    for (int e = tid; e <= E; e += kAlignThreads) offsets[e] = off[e];
+  }
+  const int nb = P_max / bm;
+  for (int b = c * kAlignThreads + tid; b < nb; b += gridDim.x * kAlignThreads) {
+    const int s0 = b * bm;
+    int be = -1;
+    if (s0 < off[E]) {
+      int lo = 0, hi = E - 1;  // largest e with off[e] <= s0
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= s0) lo = mid; else hi = mid - 1;
+      }
+      be = lo;
+    }
+    block_ids[b] = be;
+  }
+}
+
 // x_perm[p] = x[sorted[p] / k] (columns interleaved within groups of 8), zero
 // for padding slots; slots past the last used one (offsets[E]) are never read
 // by the GEMMs and are skipped. With tw (routing weight on the input) each row
@@ -236,10 +364,24 @@ moe_status_t launch_gather_f16(const uint16_t *x, int T, int k, int H, int P_max
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+int align_chunks(int R) { return R >= kAlignSplitRows ? (R + kChunkRows - 1) / kChunkRows : 0; }
+
 moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, int P_max,
                           int32_t *sorted_ids, int32_t *offsets, int32_t *block_ids, int32_t *row_pos,
-                          unsigned int *status, cudaStream_t stream, int *launches) {
-  const cudaError_t err = launch_pdl(align_kernel, dim3(1), dim3(kAlignThreads), 0, stream, ids, T * k, E, block_m,
+                          unsigned int *status, cudaStream_t stream, int *launches, int32_t *counts) {
+  const int R = T * k;
+  const int nchunks = align_chunks(R);
+  if (counts && nchunks > 0) {  // many rows: counts per chunk, then placement over many CTAs
+    cudaError_t err = launch_pdl(align_count_kernel, dim3(nchunks), dim3(kAlignThreads), 0, stream, ids, R, E, counts,
+                                 row_pos, status);
+    if (launches) ++*launches;
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    err = launch_pdl(align_place_kernel, dim3(nchunks), dim3(kAlignThreads), 0, stream, ids, R, E, block_m, P_max,
+                     nchunks, (const int32_t *)counts, sorted_ids, offsets, block_ids, row_pos);
+    if (launches) ++*launches;
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  const cudaError_t err = launch_pdl(align_kernel, dim3(1), dim3(kAlignThreads), 0, stream, ids, R, E, block_m,
                                      P_max, sorted_ids, offsets, block_ids, row_pos, status);
   if (launches) ++*launches;
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

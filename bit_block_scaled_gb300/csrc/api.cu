@@ -110,8 +110,11 @@ moe_status_t moe_align_permute(const int32_t *topk_ids, int T, int k, int E, int
                 !aligned16(block_expert_ids) || !aligned16(row_pos) || !aligned16(x_perm)))
     return MOE_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
+  // x_perm is written only by the gather, after the alignment: the many-CTA
+  // alignment keeps its per-chunk counts there meanwhile
   moe_status_t s = launch_align(topk_ids, T, k, E, block_m, P, sorted_token_ids, expert_offsets,
-                                block_expert_ids, row_pos, status_of(ws), st, &g_last_launches);
+                                block_expert_ids, row_pos, status_of(ws), st, &g_last_launches,
+                                reinterpret_cast<int32_t *>(x_perm));
   if (s != MOE_OK) return s;
   return launch_gather(x, T, k, H, P, sorted_token_ids, expert_offsets + E, x_perm, st, &g_last_launches);
 }
@@ -210,7 +213,10 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
   if (!mark(0)) return MOE_ERR_CUDA;
   if ((s = launch_route(logits, sel_bias, T, E, k, route, ids, tw, status, st, n)) != MOE_OK) return s;
   if (!mark(1)) return MOE_ERR_CUDA;
-  if ((s = launch_align(ids, T, k, E, bm, P, sorted, offs, blocks, rowpos, status, st, n)) != MOE_OK) return s;
+  // (the per-chunk counts of a many-CTA alignment live in x_perm until the gather)
+  if ((s = launch_align(ids, T, k, E, bm, P, sorted, offs, blocks, rowpos, status, st, n,
+                        reinterpret_cast<int32_t *>(xperm))) != MOE_OK)
+    return s;
   if (!mark(2)) return MOE_ERR_CUDA;
   // mul: 0 no routing weight, 1 in the GEMM2 epilogue, 2 on GEMM1's input rows
   const float *tw_in = mul == 2 ? tw : nullptr;

@@ -48,9 +48,13 @@ moe_status_t launch_route(const float *logits, const float *sel_bias, int T, int
                           int32_t *ids, float *weights, unsigned int *status, cudaStream_t stream,
                           int *launches);
 
+// counts (optional, align_chunks(T * k) * E ints): with it, batches of many
+// routed rows are aligned over many CTAs (two launches, same result).
 moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, int P_max,
                           int32_t *sorted_ids, int32_t *offsets, int32_t *block_ids, int32_t *row_pos,
-                          unsigned int *status, cudaStream_t stream, int *launches);
+                          unsigned int *status, cudaStream_t stream, int *launches, int32_t *counts = nullptr);
+// Number of row chunks the many-CTA alignment uses for R routed rows (0: one CTA).
+int align_chunks(int R);
 
 // tw (optional): the routing weight applied on the input, x row * tw[sorted[p]]
 // rounded to bf16 before it is gathered.
