@@ -14,14 +14,12 @@
 // role derives the tile coordinates by itself from expert_offsets, so roles
 // synchronise on data only. Warp roles (864 threads):
 //   warp 0        TMA producer: per tile the block scales (bulk copy, two
-//                 buffers), then per stage the packed 4-bit weight rows (and,
-//                 for wide token tiles, the token rows in the same ring slot);
-//                 it runs ahead into the next tile
-//   warp 26       narrow token tiles (decode, four K blocks per stage): the
-//                 token rows, in a ring of their own. The weight slot is then
-//                 released as soon as the dequantisation warps have read it,
-//                 not when the MMAs that read the token rows complete, so
-//                 more weight bytes stay in flight
+//                 buffers), then per stage the packed 4-bit weight rows into
+//                 the weight ring; it runs ahead into the next tile
+//   warp 26       TMA producer of the token rows, in a ring of its own. A
+//                 weight slot is released as soon as the dequantisation warps
+//                 have read it, not when the MMAs that read the token rows
+//                 complete, so the weights run further ahead
 //   warp 1        TMEM allocation; one lane issues tcgen05.mma (kind::f16, A
 //                 from TMEM, B from shared memory) into one of two TMEM
 //                 accumulators
@@ -183,19 +181,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   // 1024-byte aligned start (pointer arithmetic on the shared array keeps the
   // compiler's knowledge that all these addresses are shared memory)
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  // narrow token tiles: weights and token rows in separate rings (warp 26
-  // loads the token rows; a weight slot is freed once it has been dequantised)
-  constexpr bool SPLIT = KPB == 4;
-  const int NX = SPLIT ? p.xstages : p.stages;
+  // weights and token rows in separate rings (warp 26 loads the token rows;
+  // a weight slot is freed once it has been dequantised)
+  const int NX = p.xstages;
   const Smem L = smem_layout(p.tile_n, p.stages, KPB, p.sc_row_bytes, p.z_row_bytes, NX);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NA = p.na;                     // operand buffers in TMEM
   constexpr int kpb = KPB;                 // K blocks per pipeline stage
   constexpr uint32_t rb = 32u * KPB;       // packed bytes per weight row per stage
   const uint32_t bar0 = smem_u32(base + L.bar);
+  // full_bar / wempty_bar: weight ring slot loaded / read by its dequant group
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  // done_bar(slot): the MMAs of the stage in that ring slot have completed, so
-  // both the slot's shared memory and the stage's TMEM operand buffer are free
+  // done_bar(slot): the MMAs of the stage in that token-row ring slot have
+  // completed, so both the slot and the stage's TMEM operand buffer are free
   auto done_bar = [&](int s) { return bar0 + 8u * (kMaxStagesL + s); };
   constexpr int kB2 = 2 * kMaxStagesL, kB3 = kB2 + 2 * kMaxNA;
   auto dq_bar = [&](int s) { return bar0 + 8u * (kB2 + s); };
@@ -222,9 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   if (tid == 32) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(done_bar(s), 1);
       mbar_init(wempty_bar(s), kDqGroupThreads / 32);
+    }
+    for (int s = 0; s < NX; ++s) {
       mbar_init(xfull_bar(s), 1);
+      mbar_init(done_bar(s), 1);
     }
     for (int s = 0; s < NA; ++s) {
       mbar_init(dq_bar(s), kDqGroupThreads);
@@ -283,15 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // (the whole warp runs the loop so its control flow stays uniform; lane 0
     // issues the copies)
     const bool leader = lane == 0;
-    if (leader) {
-      prefetch_tmap(&p.tm_w);
-      prefetch_tmap(&p.tm_x);
-    }
+    if (leader) prefetch_tmap(&p.tm_w);
     const uint8_t *sc_g = static_cast<const uint8_t *>(p.scales);
     const size_t scb = (size_t)p.sc_row_bytes, zb = (size_t)p.z_row_bytes;
-    const uint32_t w_s = smem_u32(base + L.w), x_s = smem_u32(base + L.x);
+    const uint32_t w_s = smem_u32(base + L.w);
     const uint32_t sc_s = smem_u32(base + L.sc), z_s = smem_u32(base + L.z);
-    const uint32_t xstage = (uint32_t)kpb * p.tile_n * 128;
     Ring rst, rsc;
     int ntiles = 0;
     uint32_t issued_mask = 0, issued_par = 0;  // stage slots with copies in flight
@@ -324,27 +320,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       }
       rsc.advance(2);
       for (int st = 0; st < NS; ++st) {
-        ok = !((issued_mask >> rst.slot) & 1u) ||
-             mbar_wait(SPLIT ? wempty_bar(rst.slot) : done_bar(rst.slot), rst.phase ^ 1);
+        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(wempty_bar(rst.slot), rst.phase ^ 1);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
           break;
         }
         if (leader) {
-          const int kb0 = st * kpb;
-          const int nkb = min(kpb, KB - kb0);
           const uint32_t fb = full_bar(rst.slot);
-          mbar_arrive_expect_tx(fb, (64 + rows1) * rb + (SPLIT ? 0u : (uint32_t)(nkb * p.tile_n * 128)));
+          mbar_arrive_expect_tx(fb, (64 + rows1) * rb);
           const uint32_t ws = w_s + rst.slot * (kTileM * rb);
           tma_load_3d(ws, &p.tm_w, fb, st * (int)rb, wrow0, tt.e);
           if (rows1) tma_load_3d(ws + 64 * rb, &p.tm_w, fb, st * (int)rb, wrow1, tt.e);
-          const uint32_t xs0 = x_s + rst.slot * xstage;
-          // one box of tile_n token rows per K block (rows past the tile's
-          // own are loaded but never read by the MMA)
-          if (!SPLIT)
-            for (int j = 0; j < nkb; ++j)
-              tma_load_2d(xs0 + j * (p.tile_n * 128), &p.tm_x, fb, (kb0 + j) * kBK, tt.row0);
         }
         issued_mask |= 1u << rst.slot;
         issued_par = (issued_par & ~(1u << rst.slot)) | ((uint32_t)rst.phase << rst.slot);
@@ -378,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       for (int st = 0; st < NS; ++st) {
         const int kb0 = st * kpb;
         const int nkb = min(kpb, KB - kb0);
-        ok = mbar_wait(SPLIT ? xfull_bar(rs.slot) : full_bar(rs.slot), rs.phase) && mbar_wait(dq_bar(ra.slot), ra.phase);
+        ok = mbar_wait(xfull_bar(rs.slot), rs.phase) && mbar_wait(dq_bar(ra.slot), ra.phase);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -577,10 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             tmem_st16(t_a + (32u * kpb) * ca.slot + 32u * j + 16u * hk, out);
           }
         }
-        if (SPLIT) {  // this warp has read its rows of the weight slot
-          __syncwarp();
-          if (lane == 0) mbar_arrive(wempty_bar(cs.slot));
-        }
+        __syncwarp();  // this warp has read its rows of the weight slot
+        if (lane == 0) mbar_arrive(wempty_bar(cs.slot));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(dq_bar(ca.slot));
@@ -593,42 +578,40 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       rsc.advance(2);
     }
   } else if (warp == kXWarp) {
-    // ============================================================ token rows (split rings)
-    if (SPLIT) {
-      const bool leader = lane == 0;
-      if (leader) prefetch_tmap(&p.tm_x);
-      const uint32_t x_s = smem_u32(base + L.x);
-      const uint32_t xstage = (uint32_t)kpb * p.tile_n * 128;
-      Ring rx;
-      uint32_t issued_mask = 0, issued_par = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
-        for (int st = 0; st < NS; ++st) {
-          ok = !((issued_mask >> rx.slot) & 1u) || mbar_wait(done_bar(rx.slot), rx.phase ^ 1);
-          ok = __all_sync(0xffffffffu, ok && !misc[1]);
-          if (!ok) {
-            fail(leader);
-            break;
-          }
-          if (leader) {
-            const int kb0 = st * kpb;
-            const int nkb = min(kpb, KB - kb0);
-            const uint32_t fb = xfull_bar(rx.slot);
-            mbar_arrive_expect_tx(fb, (uint32_t)(nkb * p.tile_n * 128));
-            const uint32_t xs0 = x_s + rx.slot * xstage;
-            for (int j = 0; j < nkb; ++j)
-              tma_load_2d(xs0 + j * (p.tile_n * 128), &p.tm_x, fb, (kb0 + j) * kBK, tt.row0);
-          }
-          issued_mask |= 1u << rx.slot;
-          issued_par = (issued_par & ~(1u << rx.slot)) | ((uint32_t)rx.phase << rx.slot);
-          rx.advance(NX);
+    // ============================================================ token rows
+    const bool leader = lane == 0;
+    if (leader) prefetch_tmap(&p.tm_x);
+    const uint32_t x_s = smem_u32(base + L.x);
+    const uint32_t xstage = (uint32_t)kpb * p.tile_n * 128;
+    Ring rx;
+    uint32_t issued_mask = 0, issued_par = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
+      for (int st = 0; st < NS; ++st) {
+        ok = !((issued_mask >> rx.slot) & 1u) || mbar_wait(done_bar(rx.slot), rx.phase ^ 1);
+        ok = __all_sync(0xffffffffu, ok && !misc[1]);
+        if (!ok) {
+          fail(leader);
+          break;
         }
+        if (leader) {
+          const int kb0 = st * kpb;
+          const int nkb = min(kpb, KB - kb0);
+          const uint32_t fb = xfull_bar(rx.slot);
+          mbar_arrive_expect_tx(fb, (uint32_t)(nkb * p.tile_n * 128));
+          const uint32_t xs0 = x_s + rx.slot * xstage;
+          for (int j = 0; j < nkb; ++j)
+            tma_load_2d(xs0 + j * (p.tile_n * 128), &p.tm_x, fb, (kb0 + j) * kBK, tt.row0);
+        }
+        issued_mask |= 1u << rx.slot;
+        issued_par = (issued_par & ~(1u << rx.slot)) | ((uint32_t)rx.phase << rx.slot);
+        rx.advance(NX);
       }
-      if (!ok && leader)
-        for (int q = 0; q < NX; ++q)
-          if ((issued_mask >> q) & 1u) (void)mbar_wait(xfull_bar(q), (issued_par >> q) & 1u);
     }
+    if (!ok && leader)
+      for (int q = 0; q < NX; ++q)
+        if ((issued_mask >> q) & 1u) (void)mbar_wait(xfull_bar(q), (issued_par >> q) & 1u);
   } else {
     // ============================================================ epilogue
     const int q4 = warp & 3;
@@ -922,19 +905,25 @@ moe_status_t launch_grouped_gemm(int epi, const moe_qweight_t &w, const uint16_t
   a.nacc = (2 * stride + 2 * 32 * kpb <= kTmemCols) ? 2 : 1;
   a.na = (kTmemCols - a.nacc * stride) / (32 * kpb);
   if (a.na > kMaxNA) a.na = kMaxNA;
-  // stages: as many as fit in shared memory
+  // ring depths: up to four token-row slots, as many weight slots as then fit
+  // in shared memory, and never fewer weight slots than token-row slots
   const uint32_t budget = 225 * 1024;
-  int stages = kMaxStagesL;
-  const bool split = kpb == 4;
-  const int xst = split ? 4 : 0;
+  auto smem_of = [&](int st, int xs) {
+    return smem_layout(a.tile_n, st, kpb, a.sc_row_bytes, a.z_row_bytes, xs).total;
+  };
+  auto weight_slots = [&](int xs) {
+    int st = kMaxStagesL;
+    while (st > 2 && smem_of(st, xs) > budget) --st;
+    return st;
+  };
+  int xst = 4;
+  while (xst > 2 && (smem_of(weight_slots(xst), xst) > budget || weight_slots(xst) < xst)) --xst;
   a.xstages = xst;
-  while (stages > 2 && smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes, split ? xst : stages).total > budget) --stages;
-  a.stages = stages;
-  if (split && a.na > xst) a.na = xst;
+  a.stages = weight_slots(xst);
   // an operand buffer is freed by the done barrier of its previous stage's
-  // ring slot, which must not have been reused meanwhile: NA <= stages
-  if (a.na > stages) a.na = stages;
-  uint32_t smem = smem_layout(a.tile_n, stages, kpb, a.sc_row_bytes, a.z_row_bytes, split ? xst : stages).total;
+  // token-row slot, which must not have been reused meanwhile: NA <= xstages
+  if (a.na > xst) a.na = xst;
+  uint32_t smem = smem_of(a.stages, xst);
   // one CTA per SM: it allocates all of TMEM
   if (smem < 120 * 1024) smem = 120 * 1024;
   if (smem > kMaxSmem) return MOE_ERR_UNSUPPORTED;
