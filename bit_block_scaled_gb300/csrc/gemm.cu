@@ -246,8 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     tmem_alloc(smem_u32(const_cast<int *>(misc)), ncols);
     tmem_relinquish();
   }
-  // everything above overlaps the previous kernel; its outputs are read below
-  pdl_wait();
+  // Everything above overlaps the previous kernel on the stream. The token
+  // rows (x_perm, or GEMM1's output) and the per-row exponents come from that
+  // kernel: the token-row warp and the epilogue wait for it (pdl_wait) before
+  // they read them. expert_offsets comes from the alignment, which completed
+  // before the previous kernel (the gather, or GEMM1) passed its own wait and
+  // let this grid launch, so it is read here already; the weight producer and
+  // the dequantisation warps start streaming and expanding this grid's first
+  // weight tiles while the previous kernel drains.
   pdl_trigger();
   for (int i = tid; i <= p.E; i += kThreads) {
     const int v = p.expert_offsets[i];
@@ -579,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   } else if (warp == kXWarp) {
     // ============================================================ token rows
+    pdl_wait();
     const bool leader = lane == 0;
     if (leader) prefetch_tmap(&p.tm_x);
     const uint32_t x_s = smem_u32(base + L.x);
@@ -614,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if ((issued_mask >> q) & 1u) (void)mbar_wait(xfull_bar(q), (issued_par >> q) & 1u);
   } else {
     // ============================================================ epilogue
+    pdl_wait();
     const int q4 = warp & 3;
     const int eh = (warp - kFirstEpiWarp) >> 2;  // which half of the token columns
     const bool lead = warp == kFirstEpiWarp;
