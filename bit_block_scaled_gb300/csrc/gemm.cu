@@ -80,7 +80,7 @@ constexpr int kBarDq0 = 1, kBarEpi = 2, kBarDq1 = 3;
 enum { EPI_SWIGLU = 0, EPI_RELU2 = 1, EPI_WEIGHTED = 2 };
 
 struct Smem {
-  uint32_t x, w, sc, z, lut, offs, ids, tw, ex, bar, misc, total;
+  uint32_t x, w, sc, z, lut, offs, tfirst, ids, tw, ex, bar, misc, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -97,6 +97,7 @@ __host__ __device__ inline Smem smem_layout(int tile_n, int stages, int kpb, int
   s.z = o;    o += 2 * align_up(kTileM * z_row_bytes, 128);
   s.lut = o;  o += 256 * 4;
   s.offs = o; o += (kMaxE + 1) * 4;
+  s.tfirst = o; o += (kMaxE + 1) * 4;
   o = align_up(o, 16);
   s.ids = o;  o += kEpiWarps * tile_n * 4;  // one copy per epilogue warp
   s.tw = o;   o += kEpiWarps * tile_n * 4;
@@ -124,28 +125,14 @@ struct Ring {
   }
 };
 
-// Number of token tiles: each expert's slot segment split into tiles of at
-// most tile_n rows (whole warp; offs in shared memory).
-__device__ __forceinline__ int count_token_tiles(const int *offs, int E, int tile_n, int lane) {
-  int total = 0;
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    const int e = e0 + lane;
-    const int seg = e < E ? offs[e + 1] - offs[e] : 0;
-    int nt = (seg + tile_n - 1) / tile_n;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o);
-    total += nt;
-  }
-  return total;
-}
-
 struct TokenTile {
   int e, row0, nrows;
 };
 
-// Token tile number tt -> expert and slot range (whole warp).
-__device__ __forceinline__ TokenTile find_token_tile(const int *offs, int E, int tile_n, int tt, int lane) {
-  TokenTile r{0, 0, 0};
+// Token tiles: each expert's slot segment is split into tiles of at most
+// tile_n rows; tfirst[e] is the number of the expert's first token tile
+// (tfirst[E] = the count), built once per CTA by one warp.
+__device__ __forceinline__ void build_tile_table(const int *offs, int E, int tile_n, int *tfirst, int lane) {
   int cum = 0;
   for (int e0 = 0; e0 < E; e0 += 32) {
     const int e = e0 + lane;
@@ -157,19 +144,21 @@ __device__ __forceinline__ TokenTile find_token_tile(const int *offs, int E, int
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    const int excl = cum + incl - nt;
-    const unsigned m = __ballot_sync(0xffffffffu, tt >= excl && tt < excl + nt);
-    if (m) {
-      const int src = __ffs(m) - 1;
-      const int le = __shfl_sync(0xffffffffu, e, src);
-      const int lex = __shfl_sync(0xffffffffu, excl, src);
-      r.e = le;
-      r.row0 = offs[le] + (tt - lex) * tile_n;
-      r.nrows = min(tile_n, offs[le + 1] - r.row0);
-      return r;
-    }
+    if (e < E) tfirst[e] = cum + incl - nt;
     cum += __shfl_sync(0xffffffffu, incl, 31);
   }
+  if (lane == 0) tfirst[E] = cum;
+}
+
+// Token tile number tt (tt < tfirst[E], non-decreasing from call to call) ->
+// expert and slot range; e carries the expert of the previous call.
+__device__ __forceinline__ TokenTile next_token_tile(const int *offs, const int *tfirst, int tile_n, int tt,
+                                                      int &e) {
+  while (tfirst[e + 1] <= tt) ++e;
+  TokenTile r;
+  r.e = e;
+  r.row0 = offs[e] + (tt - tfirst[e]) * tile_n;
+  r.nrows = min(tile_n, offs[e + 1] - r.row0);
   return r;
 }
 
@@ -206,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   auto wempty_bar = [&](int s) { return bar0 + 8u * (kB4 + kMaxStagesL + s); };
   volatile int *misc = reinterpret_cast<volatile int *>(base + L.misc);  // [0] tmem, [1] abort
   int *offs_s = reinterpret_cast<int *>(base + L.offs);
+  int *tfirst_s = reinterpret_cast<int *>(base + L.tfirst);
   int *ids_s = reinterpret_cast<int *>(base + L.ids);
   float *tw_s = reinterpret_cast<float *>(base + L.tw);
   uint32_t *lut = reinterpret_cast<uint32_t *>(base + L.lut);
@@ -264,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (warp == 0) build_tile_table(offs_s, p.E, p.tile_n, tfirst_s, lane);
+  __syncthreads();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
   const int KB = p.K / kBK;
@@ -272,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   const bool concat = gated && p.layout == MOE_LAYOUT_CONCAT;
   const int m_tiles = p.m_tiles;
   // every role computes the same tile count and tile coordinates
-  const int total = m_tiles * count_token_tiles(offs_s, p.E, p.tile_n, lane);
+  const int total = m_tiles * tfirst_s[p.E];
   auto tile_rows = [&](int mt, int &wrow0, int &wrow1) {
     wrow0 = concat ? mt * 64 : mt * kTileM;
     wrow1 = concat ? p.I + mt * 64 : mt * kTileM + 64;
@@ -295,12 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint32_t w_s = smem_u32(base + L.w);
     const uint32_t sc_s = smem_u32(base + L.sc), z_s = smem_u32(base + L.z);
     Ring rst, rsc;
-    int ntiles = 0;
+    int ntiles = 0, te = 0;
     uint32_t issued_mask = 0, issued_par = 0;  // stage slots with copies in flight
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntiles) {
       const int mt = t % m_tiles;
-      const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
+      const TokenTile tt = next_token_tile(offs_s, tfirst_s, p.tile_n, t / m_tiles, te);
       int wrow0, wrow1;
       tile_rows(mt, wrow0, wrow1);
       const uint32_t rows1 = wrow1 < p.N ? 64 : 0;
@@ -354,10 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const bool leader = lane == 0;
     const uint32_t x_s = smem_u32(base + L.x);
     Ring rs, ra, rc;
-    int ntiles = 0;
+    int ntiles = 0, te = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntiles) {
-      const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
+      const TokenTile tt = next_token_tile(offs_s, tfirst_s, p.tile_n, t / m_tiles, te);
       const int n16 = (tt.nrows + 15) & ~15;
       const uint32_t idesc = F16 ? idesc_f16(kTileM, n16) : idesc_bf16(kTileM, n16);
       const uint32_t acc = tmem + acc_stride * rc.slot;
@@ -591,10 +583,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint32_t x_s = smem_u32(base + L.x);
     const uint32_t xstage = (uint32_t)kpb * p.tile_n * 128;
     Ring rx;
+    int te = 0;
     uint32_t issued_mask = 0, issued_par = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
+      const TokenTile tt = next_token_tile(offs_s, tfirst_s, p.tile_n, t / m_tiles, te);
       for (int st = 0; st < NS; ++st) {
         ok = !((issued_mask >> rx.slot) & 1u) || mbar_wait(done_bar(rx.slot), rx.phase ^ 1);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
@@ -632,10 +625,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // per-token 2^e of the f16 activation rows (GEMM1; else 1)
     float *gm_w = reinterpret_cast<float *>(base + L.ex) + (warp - kFirstEpiWarp) * p.tile_n;
     Ring rc;
+    int te = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const int mt = t % m_tiles;
-      const TokenTile tt = find_token_tile(offs_s, p.E, p.tile_n, t / m_tiles, lane);
+      const TokenTile tt = next_token_tile(offs_s, tfirst_s, p.tile_n, t / m_tiles, te);
       const int e = tt.e, row0 = tt.row0, nrows = tt.nrows;
       const int n16 = (nrows + 15) & ~15;
       float gmul = 1.f;
