@@ -266,103 +266,104 @@ __global__ void __launch_bounds__(kAlignThreads) align_place_kernel(const int32_
   }
 }
 
-// x_perm[p] = x[sorted[p] / k] (columns interleaved within groups of 8), zero
-// for padding slots; slots past the last used one (offsets[E]) are never read
-// by the GEMMs and are skipped. With tw (routing weight on the input) each row
-// is bf16(x * tw[sorted[p]]), the routed row's own weight.
-__global__ void __launch_bounds__(128) gather_kernel(const uint4 *__restrict__ x, int R, int k, int H8,
-                                                     const int32_t *__restrict__ sorted,
-                                                     const int32_t *__restrict__ used_end,
-                                                     uint4 *__restrict__ x_perm, const float *__restrict__ tw) {
-  pdl_wait();
-  pdl_trigger();
-  const int p = blockIdx.x;
-  if (p >= *used_end) return;
-  const int s = sorted[p];
-  uint4 *dst = x_perm + (size_t)p * H8;
-  if (s >= 0 && s < R) {
-    const uint4 *src = x + (size_t)(s / k) * H8;
-    if (tw) {
-      const float w = tw[s];
-      for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = interleave8(weigh8(src[v], w));
-    } else {
-      for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = interleave8(src[v]);
-    }
-  } else {
-    for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
-  }
-}
+// Gather, one CTA per token: the token's row is read once and written to the
+// slots of its k routed rows (row_pos); E more CTAs zero each expert's padding
+// slots (the tail of its segment whose sorted id is not a routed row). Slots
+// past offsets[E] are never read by the GEMMs and are not written.
+//   bf16 (F16 = false): x_perm[p] = x[t] with the columns interleaved within
+//     groups of 8 (the order the GEMM's weight expansion produces them in).
+//   f16 (F16 = true): x16[p] = f16(x[t] * 2^-e_p) in natural column order, with
+//     e_p chosen so that the row's largest magnitude lands in [2^14, 2^15)
+//     (exact for every bf16 element down to 2^-31 of it); xexp[p] = e_p, which
+//     the GEMM epilogue multiplies back. Padding slots get e_p = 0.
+// With tw (routing weight on the input) the row of slot p is first rounded to
+// bf16(x * tw[r]), r the routed row's own flat index.
+constexpr int kGatherMaxThreads = 512;  // one 8-column vector per thread (H <= 4096)
 
-// f16 operand path: x16[p] = f16(x[sorted[p] / k] * 2^-e_p) in natural column
-// order, with e_p chosen below so the row's largest magnitude lands in
-// [2^14, 2^15) (exact for every bf16 element down to 2^-31 of it). xexp[p] =
-// e_p; the GEMM epilogue multiplies by 2^e_p. Padding slots get zeros and
-// e_p = 0. With tw the row is first weighted as in gather_kernel.
-__global__ void __launch_bounds__(128) gather_f16_kernel(const uint4 *__restrict__ x, int R, int k, int H8,
-                                                         const int32_t *__restrict__ sorted,
-                                                         const int32_t *__restrict__ used_end,
-                                                         uint4 *__restrict__ x16, int32_t *__restrict__ xexp,
-                                                         const float *__restrict__ tw) {
-  __shared__ float wmax[4];
+template <bool F16>
+__global__ void __launch_bounds__(kGatherMaxThreads) gather_tok_kernel(
+    const uint4 *__restrict__ x, int T, int k, int H8, int E, const int32_t *__restrict__ row_pos,
+    const int32_t *__restrict__ offs, const int32_t *__restrict__ sorted, int P_max, uint4 *__restrict__ x_out,
+    int32_t *__restrict__ xexp, const float *__restrict__ tw) {
+  __shared__ float wmax[8][kGatherMaxThreads / 32];
   pdl_wait();
   pdl_trigger();
-  const int p = blockIdx.x;
-  if (p >= *used_end) return;
-  const int s = sorted[p];
-  uint4 *dst = x16 + (size_t)p * H8;
-  if (!(s >= 0 && s < R)) {
-    for (int v = threadIdx.x; v < H8; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
-    if (threadIdx.x == 0) xexp[p] = 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = T * k;
+  if ((int)blockIdx.x >= T) {  // padding slots of expert e
+    const int e = blockIdx.x - T;
+    const int lo = offs[e], hi = offs[e + 1];
+    for (int q = hi - 1; q >= lo; --q) {
+      const int sid = sorted[q];
+      if (sid >= 0 && sid < R) break;  // a routed row: the padding ends here
+      for (int v = tid; v < H8; v += blockDim.x) x_out[(size_t)q * H8 + v] = make_uint4(0, 0, 0, 0);
+      if (F16 && tid == 0) xexp[q] = 0;
+    }
     return;
   }
-  const uint4 *src = x + (size_t)(s / k) * H8;
-  const float rw = tw ? tw[s] : 1.f;
-  float m = 0.f;
-  for (int v = threadIdx.x; v < H8; v += blockDim.x) {
-    const uint4 q = tw ? weigh8(src[v], rw) : src[v];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  const int t = blockIdx.x;
+  const bool has = tid < H8;
+  const uint4 q = has ? x[(size_t)t * H8 + tid] : make_uint4(0, 0, 0, 0);
+  // one exponent per slot with tw (each slot has its own weight), else one per token
+  const int ne = F16 ? (tw ? k : 1) : 0;
+  int ex[8];
+  if (F16) {
+    const int nw = blockDim.x >> 5;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
-  }
+    for (int j = 0; j < 8; ++j) {
+      if (j < ne) {
+        const uint4 u = tw ? weigh8(q, tw[(size_t)t * k + j]) : q;
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float m = 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
-  __syncthreads();
-  m = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-  // m < 2^ex with ex from the fp32 exponent field; the row is scaled by 2^-e,
-  // e = ex - 15, so that its largest entry lands in [2^14, 2^15): below the f16
-  // maximum, and every bf16 entry down to 2^-31 of the row's largest stays
-  // exact in f16 (normal down to 2^-28 of it, subnormal with 8 bits below)
-  const int ex = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 126;
-  const int e = max(-126, min(ex - 15, 126));
-  const float sc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-  for (int v = threadIdx.x; v < H8; v += blockDim.x) {
-    const uint4 q = tw ? weigh8(src[v], rw) : src[v];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    uint32_t o[4];
+        for (int i = 0; i < 4; ++i)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * sc, __uint_as_float(w[i] & 0xFFFF0000u) * sc);
-      o[i] = *reinterpret_cast<const uint32_t *>(&h);
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) wmax[j][warp] = m;
+      }
     }
-    dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < ne) {
+        float m = 0.f;
+        for (int w = 0; w < nw; ++w) m = fmaxf(m, wmax[j][w]);
+        // m < 2^x (x from the fp32 exponent field); scaling by 2^-e, e = x - 15,
+        // puts the largest entry in [2^14, 2^15): below the f16 maximum, and
+        // every bf16 entry down to 2^-31 of it stays exact in f16 (normal down
+        // to 2^-28 of it, subnormal with 8 bits below)
+        const int xe = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 126;
+        ex[j] = max(-126, min(xe - 15, 126));
+      }
+    }
   }
-  if (threadIdx.x == 0) xexp[p] = min(e, 126);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= k) break;
+    const int r = t * k + j;
+    const int p = row_pos[r];
+    if (p < 0 || p >= P_max) continue;  // a row with a bad expert id is not placed
+    const uint4 u = tw ? weigh8(q, tw[r]) : q;
+    if (F16) {
+      const int e = tw ? ex[j] : ex[0];
+      const float sc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * sc, __uint_as_float(w[i] & 0xFFFF0000u) * sc);
+        o[i] = *reinterpret_cast<const uint32_t *>(&h);
+      }
+      if (has) x_out[(size_t)p * H8 + tid] = make_uint4(o[0], o[1], o[2], o[3]);
+      if (tid == 0) xexp[p] = e;
+    } else {
+      if (has) x_out[(size_t)p * H8 + tid] = interleave8(u);
+    }
+  }
 }
 
 }  // namespace
-
-moe_status_t launch_gather_f16(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
-                               const int32_t *offsets_end, uint16_t *x16, int32_t *xexp, cudaStream_t stream,
-                               int *launches, const float *tw) {
-  if (P_max == 0) return MOE_OK;
-  const cudaError_t err = launch_pdl(gather_f16_kernel, dim3(P_max), dim3(128), 0, stream,
-                                     reinterpret_cast<const uint4 *>(x), T * k, k, H / 8, sorted_ids, offsets_end,
-                                     reinterpret_cast<uint4 *>(x16), xexp, tw);
-  if (launches) ++*launches;
-  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
 
 int align_chunks(int R) { return R >= kAlignSplitRows ? (R + kChunkRows - 1) / kChunkRows : 0; }
 
@@ -387,13 +388,17 @@ moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, 
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
-                           const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches,
-                           const float *tw) {
-  if (P_max == 0) return MOE_OK;
-  const cudaError_t err = launch_pdl(gather_kernel, dim3(P_max), dim3(128), 0, stream,
-                                     reinterpret_cast<const uint4 *>(x), T * k, k, H / 8, sorted_ids, offsets_end,
-                                     reinterpret_cast<uint4 *>(x_perm), tw);
+moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int E, int P_max, const int32_t *row_pos,
+                           const int32_t *offsets, const int32_t *sorted_ids, uint16_t *x_out, int32_t *xexp,
+                           bool f16, cudaStream_t stream, int *launches, const float *tw) {
+  if (T == 0 || P_max == 0) return MOE_OK;
+  const int H8 = H / 8;
+  const int threads = (H8 + 31) / 32 * 32;
+  if (threads > kGatherMaxThreads || k > 8) return MOE_ERR_UNSUPPORTED;
+  const auto kern = f16 ? gather_tok_kernel<true> : gather_tok_kernel<false>;
+  const cudaError_t err = launch_pdl(kern, dim3(T + E), dim3(threads), 0, stream, reinterpret_cast<const uint4 *>(x),
+                                     T, k, H8, E, row_pos, offsets, sorted_ids, P_max,
+                                     reinterpret_cast<uint4 *>(x_out), xexp, tw);
   if (launches) ++*launches;
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -116,7 +116,8 @@ moe_status_t moe_align_permute(const int32_t *topk_ids, int T, int k, int E, int
                                 block_expert_ids, row_pos, status_of(ws), st, &g_last_launches,
                                 reinterpret_cast<int32_t *>(x_perm));
   if (s != MOE_OK) return s;
-  return launch_gather(x, T, k, H, P, sorted_token_ids, expert_offsets + E, x_perm, st, &g_last_launches);
+  return launch_gather(x, T, k, H, E, P, row_pos, expert_offsets, sorted_token_ids, x_perm, nullptr, false, st,
+                       &g_last_launches);
 }
 
 moe_status_t moe_grouped_gemm1_act(const uint16_t *x_perm, const int32_t *sorted_token_ids,
@@ -220,8 +221,7 @@ static moe_status_t forward_impl(const uint16_t *x, const float *logits, const f
   if (!mark(2)) return MOE_ERR_CUDA;
   // mul: 0 no routing weight, 1 in the GEMM2 epilogue, 2 on GEMM1's input rows
   const float *tw_in = mul == 2 ? tw : nullptr;
-  s = f16_1 ? launch_gather_f16(x, T, k, H, P, sorted, offs + E, xperm, xexp, st, n, tw_in)
-          : launch_gather(x, T, k, H, P, sorted, offs + E, xperm, st, n, tw_in);
+  s = launch_gather(x, T, k, H, E, P, rowpos, offs, sorted, xperm, xexp, f16_1 != 0, st, n, tw_in);
   if (s != MOE_OK) return s;
   if (!mark(3)) return MOE_ERR_CUDA;
   const int epi1 = act.kind == MOE_ACT_SWIGLUOAI ? 0 : 1;

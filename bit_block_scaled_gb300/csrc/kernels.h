@@ -56,15 +56,14 @@ moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, 
 // Number of row chunks the many-CTA alignment uses for R routed rows (0: one CTA).
 int align_chunks(int R);
 
-// tw (optional): the routing weight applied on the input, x row * tw[sorted[p]]
-// rounded to bf16 before it is gathered.
-moe_status_t launch_gather_f16(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
-                               const int32_t *offsets_end, uint16_t *x16, int32_t *xexp, cudaStream_t stream,
-                               int *launches, const float *tw = nullptr);
-
-moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int P_max, const int32_t *sorted_ids,
-                           const int32_t *offsets_end, uint16_t *x_perm, cudaStream_t stream, int *launches,
-                           const float *tw = nullptr);
+// Token rows into the slots of their routed rows (row_pos), padding slots
+// (found from offsets and sorted_ids) zeroed. f16: power-of-two scaled f16
+// rows in natural column order with their exponents in xexp; else bf16 rows
+// with the columns interleaved within groups of 8. tw (optional): the routing
+// weight applied on the input, each slot's row rounded to bf16(x * tw[r]).
+moe_status_t launch_gather(const uint16_t *x, int T, int k, int H, int E, int P_max, const int32_t *row_pos,
+                           const int32_t *offsets, const int32_t *sorted_ids, uint16_t *x_out, int32_t *xexp,
+                           bool f16, cudaStream_t stream, int *launches, const float *tw = nullptr);
 
 // moe_forward with a fixed device workspace (moe_forward_static): all host
 // checks before anything is enqueued, then clear the status word, run the

@@ -20,11 +20,11 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4 v) {
   }
 }
 
-constexpr int kUnpermThreads = 64;  // one 8-column vector per thread
+constexpr int kUnpermMaxThreads = 512;  // one 8-column vector per thread (H <= 4096)
 
-// grid (T, ceil(H/8 / 64)): each CTA covers 512 columns of one token, so even
-// a small batch spreads over many SMs
-__global__ void __launch_bounds__(kUnpermThreads) unpermute_kernel(const uint4 *__restrict__ y,
+// grid (T, ceil(H/8 / threads)): one token per CTA (a small batch, T < 256,
+// splits each row over CTAs of 64 threads so that it still spreads over the SMs)
+__global__ void __launch_bounds__(kUnpermMaxThreads) unpermute_kernel(const uint4 *__restrict__ y,
                                                                    const int32_t *__restrict__ row_pos, int T,
                                                                    int k, int H8, int P_max,
                                                                    uint4 *__restrict__ out, unsigned int *status) {
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kUnpermThreads) unpermute_kernel(const uint4 *
     }
   }
   if (!ok && threadIdx.x == 0 && blockIdx.y == 0) raise_status(status, MOE_ERR_BAD_INDEX);
-  const int v = blockIdx.y * kUnpermThreads + threadIdx.x;
+  const int v = blockIdx.y * blockDim.x + threadIdx.x;
   if (v < H8) {
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -64,8 +64,11 @@ moe_status_t launch_unpermute(const uint16_t *y, const int32_t *row_pos, int T, 
                               uint16_t *out, unsigned int *status, cudaStream_t stream, int *launches) {
   if (T == 0) return MOE_OK;
   const int H8 = H / 8;
-  const dim3 grid(T, (H8 + kUnpermThreads - 1) / kUnpermThreads);
-  const cudaError_t err = launch_pdl(unpermute_kernel, grid, dim3(kUnpermThreads), 0, stream,
+  int threads = (H8 + 31) / 32 * 32;
+  if (threads > kUnpermMaxThreads) return MOE_ERR_UNSUPPORTED;
+  if (T < 256) threads = 64;
+  const dim3 grid(T, (H8 + threads - 1) / threads);
+  const cudaError_t err = launch_pdl(unpermute_kernel, grid, dim3(threads), 0, stream,
                                      reinterpret_cast<const uint4 *>(y), row_pos, T, k, H8, P_max,
                                      reinterpret_cast<uint4 *>(out), status);
   if (launches) ++*launches;
