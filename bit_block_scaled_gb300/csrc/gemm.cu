@@ -173,6 +173,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   // weights and token rows in separate rings (warp 26 loads the token rows;
   // a weight slot is freed once it has been dequantised)
   const int NX = p.xstages;
+  // INT4 (the costliest expansion): each stage is expanded and handed to the
+  // MMA warp in two halves of its K blocks, so the MMAs of the first half run
+  // while the second half is expanded (c2 GEMM1 498 -> 467 us). The FP4
+  // expansions are fast enough that the extra TMEM-store wait costs more.
+  constexpr bool HALVES = FMT == MOE_FMT_INT4;
+  constexpr int NH = HALVES ? 2 : 1;
   const Smem L = smem_layout(p.tile_n, p.stages, KPB, p.sc_row_bytes, p.z_row_bytes, NX);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NA = p.na;                     // operand buffers in TMEM
@@ -185,7 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   // completed, so both the slot and the stage's TMEM operand buffer are free
   auto done_bar = [&](int s) { return bar0 + 8u * (kMaxStagesL + s); };
   constexpr int kB2 = 2 * kMaxStagesL, kB3 = kB2 + 2 * kMaxNA;
-  auto dq_bar = [&](int s) { return bar0 + 8u * (kB2 + s); };
+  // dq_bar(slot, h): the stage in operand buffer slot is expanded (h = 0), or,
+  // for INT4, half h of its K blocks is
+  auto dq_bar = [&](int s, int h) { return bar0 + 8u * (kB2 + 2 * s + h); };
   auto scfull_bar = [&](int s) { return bar0 + 8u * (kB3 + s); };
   auto scempty_bar = [&](int s) { return bar0 + 8u * (kB3 + 2 + s); };
   auto accfull_bar = [&](int s) { return bar0 + 8u * (kB3 + 4 + s); };
@@ -217,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(done_bar(s), 1);
     }
     for (int s = 0; s < NA; ++s) {
-      mbar_init(dq_bar(s), kDqGroupThreads);
+      mbar_init(dq_bar(s, 0), kDqGroupThreads);
+      mbar_init(dq_bar(s, 1), kDqGroupThreads);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(scfull_bar(s), 1);
@@ -363,31 +372,36 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       for (int st = 0; st < NS; ++st) {
         const int kb0 = st * kpb;
         const int nkb = min(kpb, KB - kb0);
-        ok = mbar_wait(xfull_bar(rs.slot), rs.phase) && mbar_wait(dq_bar(ra.slot), ra.phase);
-        ok = __all_sync(0xffffffffu, ok && !misc[1]);
+        // operands computed by the whole warp (warp-uniform values), issued by
+        // one elected lane (INT4: each half of the K blocks once expanded)
+        const uint32_t aa = tmem + a_col + (32u * kpb) * ra.slot;
+        const uint32_t xb = x_s + rs.slot * kpb * (p.tile_n * 128);
+        const uint32_t db = done_bar(rs.slot);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          ok = (h || mbar_wait(xfull_bar(rs.slot), rs.phase)) && mbar_wait(dq_bar(ra.slot, h), ra.phase);
+          ok = __all_sync(0xffffffffu, ok && !misc[1]);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int jj = 0; jj < kpb / NH; ++jj) {
+              const int j = h * (kpb / NH) + jj;
+              if (j < nkb) {
+                const uint64_t bd = smem_desc_sw128(xb + j * (p.tile_n * 128));
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                  umma_bf16_ts(acc, aa + 32u * j + 8u * kk, bd + 2u * kk, idesc, (kb0 + j + kk) != 0);
+              }
+            }
+            if (h == NH - 1) umma_commit(db);  // one commit frees the ring slot and the operand buffer
+          }
+          __syncwarp();
+        }
         if (!ok) {
           fail(leader);
           break;
         }
-        tc_fence_after();
-        // operands computed by the whole warp (warp-uniform values), issued by
-        // one elected lane
-        const uint32_t aa = tmem + a_col + (32u * kpb) * ra.slot;
-        const uint32_t xb = x_s + rs.slot * kpb * (p.tile_n * 128);
-        const uint32_t db = done_bar(rs.slot);
-        if (elect_one()) {
-#pragma unroll
-          for (int j = 0; j < kpb; ++j) {
-            if (j < nkb) {
-              const uint64_t bd = smem_desc_sw128(xb + j * (p.tile_n * 128));
-#pragma unroll
-              for (int kk = 0; kk < kBK / 16; ++kk)
-                umma_bf16_ts(acc, aa + 32u * j + 8u * kk, bd + 2u * kk, idesc, (kb0 + j + kk) != 0);
-            }
-          }
-          umma_commit(db);  // one commit frees the ring slot and the operand buffer
-        }
-        __syncwarp();
         ra.advance(NA);
         rs.advance(NX);
       }
@@ -499,8 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         } else
 #pragma unroll
         for (int i = 0; i < nw; ++i) {
-          const int ch = kq * nw + i;  // 16-byte chunk of the row: K block ch / 2, half ch % 2
+          // 16-byte chunk of the row: K block ch / 2, half ch % 2. INT4: the
+          // first half of the stage's chunks first, split between the lane
+          // quarter's two warps, then the second half
+          const int ch = HALVES ? (i / (nw / 2)) * nw + kq * (nw / 2) + i % (nw / 2) : kq * nw + i;
           const int j = ch >> 1, hk = ch & 1;
+          if (HALVES && i == nw / 2) {  // the first half is in TMEM: hand it to the MMA warp
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(dq_bar(ca.slot, 0));
+          }
           if (j < nkb) {
             const int kb = kb0 + j;
             uint32_t out[16];
@@ -566,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (lane == 0) mbar_arrive(wempty_bar(cs.slot));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(dq_bar(ca.slot));
+        mbar_arrive(dq_bar(ca.slot, NH - 1));
         ca.advance(NA);
         cs.advance(p.stages);
         if (kdone >= NA) cl.advance(NX);
