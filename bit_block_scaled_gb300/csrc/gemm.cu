@@ -12,11 +12,12 @@
 // The kernel is persistent, one CTA per SM (it takes all 512 TMEM columns):
 // each CTA walks the tiles blockIdx.x, blockIdx.x + gridDim.x, ... and every
 // role derives the tile coordinates by itself from expert_offsets, so roles
-// synchronise on data only. Warp roles (864 threads):
+// synchronise on data only. Warp roles (864 threads for wide token tiles,
+// 736 for the narrow tiles of decode):
 //   warp 0        TMA producer: per tile the block scales (bulk copy, two
 //                 buffers), then per stage the packed 4-bit weight rows into
 //                 the weight ring; it runs ahead into the next tile
-//   warp 26       TMA producer of the token rows, in a ring of its own. A
+//   warp 26 / 22  TMA producer of the token rows, in a ring of its own. A
 //                 weight slot is released as soon as the dequantisation warps
 //                 have read it, not when the MMAs that read the token rows
 //                 complete, so the weights run further ahead
@@ -27,8 +28,8 @@
 //                 warp w owns TMEM lanes 32*(w%4).. (one weight row per lane)
 //                 and half of its group's stage K range
 //   warps 18..25  epilogue of the previous tile's accumulator while the next
-//                 tile is being computed (two warps per TMEM lane quarter, one
-//                 per half of the token columns)
+//   (18..21)      tile is being computed (two warps per TMEM lane quarter, one
+//                 per half of the token columns; one per quarter for decode)
 // The epilogues: GEMM1 adds bias and applies swigluoai (gate/up pairs are
 // adjacent TMEM lanes) or ReLU^2; GEMM2 adds bias and multiplies each token row
 // by its own routing weight, read through that row's flat index (the failure
@@ -60,13 +61,18 @@ namespace moe4 {
 namespace {
 
 constexpr int kFirstDqWarp = 2, kDqWarps = 16;
-constexpr int kFirstEpiWarp = kFirstDqWarp + kDqWarps, kEpiWarps = 8;
-constexpr int kXWarp = kFirstEpiWarp + kEpiWarps;  // token-row producer of the split rings
-constexpr int kWarps = kXWarp + 1;
-constexpr int kThreads = kWarps * 32;
+constexpr int kFirstEpiWarp = kFirstDqWarp + kDqWarps;
 constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kDqGroupThreads = kDqThreads / 2;  // one of the two dequant groups
-constexpr int kEpiThreads = kEpiWarps * 32;
+// Epilogue warps: 8 (two per TMEM lane quarter, one per half of the token
+// columns) for the wide token tiles of prefill (KPB = 2), 4 for the narrow
+// tiles of decode (KPB = 4), whose 16-32 token columns one warp per quarter
+// drains in time; the smaller CTA also leaves the decode kernel more
+// registers per thread (c1 GEMM1 88 -> 82 us in one comparison run). The
+// token-row producer follows the epilogue warps.
+__host__ __device__ constexpr int epi_warps(int kpb) { return kpb == 4 ? 4 : 8; }
+__host__ __device__ constexpr int x_warp(int kpb) { return kFirstEpiWarp + epi_warps(kpb); }
+__host__ __device__ constexpr int cta_threads(int kpb) { return (x_warp(kpb) + 1) * 32; }
 constexpr int kTileM = 128;       // weight rows per tile (TMEM lanes)
 constexpr int kBK = 64;           // K per MMA block (128 bytes of bf16)
 constexpr int kTmemCols = 512;    // the whole tensor memory of the SM
@@ -99,9 +105,9 @@ __host__ __device__ inline Smem smem_layout(int tile_n, int stages, int kpb, int
   s.offs = o; o += (kMaxE + 1) * 4;
   s.tfirst = o; o += (kMaxE + 1) * 4;
   o = align_up(o, 16);
-  s.ids = o;  o += kEpiWarps * tile_n * 4;  // one copy per epilogue warp
-  s.tw = o;   o += kEpiWarps * tile_n * 4;
-  s.ex = o;   o += kEpiWarps * tile_n * 4;
+  s.ids = o;  o += epi_warps(kpb) * tile_n * 4;  // one copy per epilogue warp
+  s.tw = o;   o += epi_warps(kpb) * tile_n * 4;
+  s.ex = o;   o += epi_warps(kpb) * tile_n * 4;
   o = align_up(o, 8);
   s.bar = o;  o += (4 * kMaxStagesL + 2 * kMaxNA + 8) * 8;
   s.misc = o; o += 64;
@@ -165,12 +171,14 @@ __device__ __forceinline__ TokenTile next_token_tile(const int *offs, const int 
 }  // namespace
 
 template <int FMT, int EPI, int KPB, bool F16>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+__global__ void __launch_bounds__(cta_threads(KPB), 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+  constexpr int kEpiWarps = epi_warps(KPB), kEpiThreads = kEpiWarps * 32;
+  constexpr int kXWarp = x_warp(KPB), kThreads = cta_threads(KPB);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned start (pointer arithmetic on the shared array keeps the
   // compiler's knowledge that all these addresses are shared memory)
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  // weights and token rows in separate rings (warp 26 loads the token rows;
+  // weights and token rows in separate rings (kXWarp loads the token rows;
   // a weight slot is freed once it has been dequantised)
   const int NX = p.xstages;
   // INT4 (the costliest expansion): each stage is expanded and handed to the
@@ -638,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // ============================================================ epilogue
     pdl_wait();
     const int q4 = warp & 3;
-    const int eh = (warp - kFirstEpiWarp) >> 2;  // which half of the token columns
+    const int eh = (warp - kFirstEpiWarp) >> 2;  // which part of the token columns
     const bool lead = warp == kFirstEpiWarp;
     const int r = q4 * 32 + lane;  // weight row in the tile == TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -699,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       }
       tc_fence_after();
       const uint32_t ta = t_lane + acc_stride * rc.slot;
-      for (int c0 = 16 * eh; c0 < n16; c0 += 32) {
+      for (int c0 = 16 * eh; c0 < n16; c0 += 16 * (kEpiWarps / 4)) {
         uint32_t v[16];
         tmem_ld16(ta + c0, v);
         // which of these 16 tokens are stored (one shared-memory read per lane)
@@ -829,7 +837,7 @@ moe_status_t launch_t(const GemmArgs &a, dim3 grid, uint32_t smem, cudaStream_t 
       return MOE_ERR_CUDA;
     done.store(1, std::memory_order_release);
   }
-  return launch_pdl(kern, grid, dim3(kThreads), smem, st, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_pdl(kern, grid, dim3(cta_threads(KPB)), smem, st, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
