@@ -149,7 +149,10 @@ moe_status_t moe_route_topk(const float *logits, const float *sel_bias, int T,
  *   row_pos          int32 [T*k]     slot of each flat row
  *   x_perm           bf16  [P_max][H] x[sorted/k] per slot, zero in padding,
  *                    columns interleaved within every group of 8 (below)
- * An expert id outside [0, E) latches MOE_ERR_BAD_INDEX and is dropped.
+ * An expert id outside [0, E) latches MOE_ERR_BAD_INDEX and is dropped
+ * (row_pos = -1). Rows of x_perm at and past expert_offsets[E] are left
+ * unspecified (from 4096 routed rows on, the call keeps per-chunk expert
+ * counts at the start of x_perm until it writes the rows).
  * Interleaved columns: x_perm and a_out (below) store the columns of each
  * group of 8 in the order 0,4,1,5,2,6,3,7 -- the order in which the GEMMs
  * expand the packed 4-bit weights -- so stored column 8g+q holds column
