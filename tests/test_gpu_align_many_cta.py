@@ -108,3 +108,24 @@ def test_bad_ids_in_a_large_batch_latch_status_and_skip_the_row():
         assert np.all(seg[rows.size:] == R)
         assert np.array_equal(g["row_pos"][rows], g["offs"][e] + np.arange(rows.size))
     assert np.all(g["sorted"][g["offs"][-1]:] == R)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "int4"])
+@pytest.mark.parametrize("mul", [1, 2])
+def test_forward_large_batch_matches_oracle(fmt, mul):
+    """moe_forward over 6,000 routed rows (the many-CTA alignment, the
+    per-token gather with the routing weight on the input rows or in the
+    GEMM2 epilogue), every output element against the oracle."""
+    import bit_block_scaled_gb300 as moe
+    from gpu_helpers import act_of, assert_close, get_config, gpu_steps, make, oracle_full
+    cfg = get_config("c0", name=f"large_{fmt}_{mul}", fmt=fmt, H=256, I=256, E=32, T=1500, k=4)
+    L, N = make(cfg, seed=41)
+    g = gpu_steps(L, cfg)
+    ws = torch.zeros(moe.moe_workspace_size(cfg.T, cfg.E, cfg.k, cfg.H, cfg.I, 16), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(L["x"], L["logits"], L["sel_bias"], cfg.k, moe.ROUTE[cfg.route], L["w13"], L["w2"], 0,
+                    act_of(cfg), mul, 16, out, ws)
+    assert moe.moe_read_status(ws) == 0
+    o = oracle_full(N, cfg, ids=g["topk_ids"].astype(np.int32), tw=g["topk_weights"], mul=mul)
+    assert_close(out.float().cpu().numpy(), o["out"], f"large batch out ({fmt}, mul {mul})")
