@@ -853,10 +853,11 @@ int choose_tile_n(int num_rows, int E) {
   int n = ((2 * avg + 15) / 16) * 16;
   if (n < 16) n = 16;
   // wider tiles amortise each dequantised weight tile over more tokens: 192
-  // rows (two accumulators next to two operand buffers in TMEM) when the
-  // experts are full enough to fill them, else 160 (three operand buffers),
-  // which also keeps unevenly loaded experts of up to 160 rows in one tile
-  if (n > 128) n = avg >= 160 ? 192 : 160;
+  // rows (two accumulators next to two operand buffers in TMEM) when that
+  // cuts the token tiles of an average expert, else 160 (three operand
+  // buffers), which also keeps unevenly loaded experts of up to 160 rows in
+  // one tile
+  if (n > 128) n = ((avg + 159) / 160 == (avg + 191) / 192) ? 160 : 192;
   return n;
 }
 
