@@ -105,9 +105,9 @@ __host__ __device__ inline Smem smem_layout(int tile_n, int stages, int kpb, int
   s.offs = o; o += (kMaxE + 1) * 4;
   s.tfirst = o; o += (kMaxE + 1) * 4;
   o = align_up(o, 16);
-  s.ids = o;  o += epi_warps(kpb) * tile_n * 4;  // one copy per epilogue warp
-  s.tw = o;   o += epi_warps(kpb) * tile_n * 4;
-  s.ex = o;   o += epi_warps(kpb) * tile_n * 4;
+  s.ids = o;  o += 2 * tile_n * 4;  // one buffer per TMEM accumulator
+  s.tw = o;   o += 2 * tile_n * 4;
+  s.ex = o;   o += 2 * tile_n * 4;
   o = align_up(o, 8);
   s.bar = o;  o += (4 * kMaxStagesL + 2 * kMaxNA + 8) * 8;
   s.misc = o; o += 64;
@@ -650,10 +650,7 @@ __global__ void __launch_bounds__(cta_threads(KPB), 1) grouped_gemm_kernel(const
     const bool lead = warp == kFirstEpiWarp;
     const int r = q4 * 32 + lane;  // weight row in the tile == TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
-    int *ids_w = ids_s + (warp - kFirstEpiWarp) * p.tile_n;  // this warp's copy of the row ids
-    float *tw_w = tw_s + (warp - kFirstEpiWarp) * p.tile_n;
-    // per-token 2^e of the f16 activation rows (GEMM1; else 1)
-    float *gm_w = reinterpret_cast<float *>(base + L.ex) + (warp - kFirstEpiWarp) * p.tile_n;
+    const int etid = tid - kFirstEpiWarp * 32;  // thread index within the epilogue warps
     Ring rc;
     int te = 0;
     bool ok = true;
@@ -668,9 +665,15 @@ __global__ void __launch_bounds__(cta_threads(KPB), 1) grouped_gemm_kernel(const
       const float afold = (F16 && EPI == EPI_WEIGHTED) ? 0x1p-9f : 1.f;
       if (FMT == MOE_FMT_NVFP4) gmul = F16 ? p.gscale[e] * afold : p.gscale[e] * 256.f;
       if (FMT == MOE_FMT_MXFP4 && F16) gmul = 0x1p-12f * afold;
-      // this tile's row ids, routing weights and multipliers, staged per warp
-      __syncwarp();
-      for (int i = lane; i < n16; i += 32) {
+      // this tile's row ids, routing weights and per-token 2^e of the f16
+      // activation rows, staged by all epilogue warps into the buffer of
+      // this tile's accumulator; the barrier below publishes them, and the
+      // buffer's previous tile was finished by every warp before the
+      // barrier of the tile in between
+      int *ids_w = ids_s + rc.slot * p.tile_n;
+      float *tw_w = tw_s + rc.slot * p.tile_n;
+      float *gm_w = reinterpret_cast<float *>(base + L.ex) + rc.slot * p.tile_n;
+      for (int i = etid; i < n16; i += kEpiThreads) {
         int sid = p.num_rows;
         if (i < nrows) sid = p.sorted_ids[row0 + i];
         ids_w[i] = sid;
@@ -681,7 +684,6 @@ __global__ void __launch_bounds__(cta_threads(KPB), 1) grouped_gemm_kernel(const
         if (F16 && EPI != EPI_WEIGHTED && i < nrows) gm = __uint_as_float((uint32_t)(127 + p.xexp[row0 + i]) << 23);
         gm_w[i] = gm;
       }
-      __syncwarp();
       int n_w, col;
       bool col_ok;
       if (gated) {
