@@ -170,7 +170,12 @@ moe_status_t moe_align_permute(const int32_t *topk_ids, int T, int k, int E,
  * x_perm is read and a_out written with interleaved columns (see
  * moe_align_permute).
  * W13' is the bf16 dequantised operand. Padding slots of a_out are not written.
- * P_max must be moe_padded_rows(...) of the align call that made the metadata. */
+ * P_max must be moe_padded_rows(...) of the align call that made the metadata.
+ * Both grouped GEMMs start streaming weights while the previous kernel on the
+ * stream drains (programmatic dependent launch); they wait for it before
+ * reading x_perm / a, but read expert_offsets at once: it must not be written
+ * by that previous kernel (moe_align_permute's last kernel is its gather, so
+ * the step sequence above satisfies this). */
 moe_status_t moe_grouped_gemm1_act(const uint16_t *x_perm,
                                    const int32_t *sorted_token_ids,
                                    const int32_t *expert_offsets, int P_max,
