@@ -417,7 +417,8 @@ def run_ours(args):
     # per-kernel breakdown: moe_forward_profile's events around each launch
     bd = breakdown(layer, flush, args.breakdown_iters)
 
-    # end to end through the C ABI with host buffers (pinned), copies inside
+    # end to end through the C ABI with host buffers (pinned: the kernels read
+    # x and logits and write out over the host link inside the timed region)
     xh = L["x"].cpu().pin_memory()
     lh = L["logits"].cpu().pin_memory()
     oh = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()

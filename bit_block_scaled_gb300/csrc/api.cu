@@ -318,6 +318,20 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *logits_host, 
   if (!x_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;
   const Carve c = carve(T, E, k, H, I, block_m);
   cudaStream_t st = (cudaStream_t)stream;
+  // Page-locked host buffers are mapped into the device's address space: the
+  // route and gather kernels then read x and logits, and the unpermute writes
+  // out, in place over the host link (NVLink-C2C on a Grace host), with no
+  // staging copies. Other host memory is staged through the workspace.
+  void *xm = nullptr, *lm = nullptr, *om = nullptr;
+  const bool mapped = cudaHostGetDevicePointer(&xm, const_cast<uint16_t *>(x_host), 0) == cudaSuccess &&
+                      cudaHostGetDevicePointer(&lm, const_cast<float *>(logits_host), 0) == cudaSuccess &&
+                      cudaHostGetDevicePointer(&om, out_host, 0) == cudaSuccess && aligned16(xm) &&
+                      aligned16(lm) && aligned16(om);
+  if (!mapped) (void)cudaGetLastError();  // a pageable buffer: not an error
+  if (mapped)
+    return forward_impl(static_cast<const uint16_t *>(xm), static_cast<const float *>(lm), sel_bias, T, E, k, H, I,
+                        route, w13, w2, gate_up_layout, act, mul_topk_weights, block_m,
+                        static_cast<uint16_t *>(om), ws, st);
   uint16_t *xd = at<uint16_t>(ws, c.xin);
   float *ld = at<float>(ws, c.lin);
   uint16_t *od = at<uint16_t>(ws, c.outb);

@@ -225,10 +225,12 @@ moe_status_t moe_forward(const uint16_t *x, const float *logits,
                          uint16_t *out, void *ws, size_t ws_bytes,
                          moe_stream_t stream);
 
-/* moe_forward with x, logits and out in HOST memory (pinned for overlap):
- * copies x and logits in, runs the layer, copies out back, all on `stream`;
- * weights and ws stay in device memory. Returns after enqueueing; the caller
- * synchronises the stream before reading out. */
+/* moe_forward with x, logits and out in HOST memory; weights and ws stay in
+ * device memory. Page-locked (pinned, hence mapped) buffers are read and
+ * written in place by the kernels over the host link, with no staging
+ * copies; pageable ones are copied in through the workspace and out back on
+ * `stream`. Returns after enqueueing; the caller synchronises the stream
+ * before reading out. */
 moe_status_t moe_forward_host(const uint16_t *x_host, const float *logits_host,
                               const float *sel_bias, int T, int E, int k, int H,
                               int I, int route, const moe_qweight_t *w13,
