@@ -130,3 +130,22 @@ def test_forward_large_batch_matches_oracle(fmt, mul, T):
     assert moe.moe_read_status(ws) == 0
     o = oracle_full(N, cfg, ids=g["topk_ids"].astype(np.int32), tw=g["topk_weights"], mul=mul)
     assert_close(out.float().cpu().numpy(), o["out"], f"large batch out ({fmt}, mul {mul})")
+
+
+def test_forward_widest_rows_one_cta_per_token():
+    """H = 4096 (512 vectors of 8 columns, the widest row) at 300 tokens: the
+    gather and the unpermute each run one 512-thread CTA per token."""
+    import bit_block_scaled_gb300 as moe
+    from gpu_helpers import act_of, assert_close, get_config, gpu_steps, make, oracle_full
+    cfg = get_config("c0", name="wide_rows", fmt="nvfp4", H=4096, I=128, E=8, T=300, k=2)
+    L, N = make(cfg, seed=43)
+    g = gpu_steps(L, cfg)
+    ws = torch.zeros(moe.moe_workspace_size(cfg.T, cfg.E, cfg.k, cfg.H, cfg.I, 16), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(L["x"], L["logits"], L["sel_bias"], cfg.k, moe.ROUTE[cfg.route], L["w13"], L["w2"], 0,
+                    act_of(cfg), 1, 16, out, ws)
+    assert moe.moe_read_status(ws) == 0
+    o = oracle_full(N, cfg, ids=g["topk_ids"].astype(np.int32), tw=g["topk_weights"])
+    assert_close(g["out"], o["out"], "wide rows, steps")
+    assert_close(out.float().cpu().numpy(), o["out"], "wide rows, forward")
