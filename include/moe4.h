@@ -146,6 +146,9 @@ moe_status_t moe_route_topk(const float *logits, const float *sel_bias, int T,
  *   sorted_token_ids int32 [P_max]   flat row of each slot (T*k = padding)
  *   expert_offsets   int32 [E+1]     first slot of each expert; [E] = used slots
  *   block_expert_ids int32 [P_max/block_m]  expert of each block, -1 unused
+ *                    (the pages' moe_align_block_size output, for callers
+ *                    that schedule by block; the grouped GEMMs below walk
+ *                    expert_offsets instead and do not read it)
  *   row_pos          int32 [T*k]     slot of each flat row
  *   x_perm           bf16  [P_max][H] x[sorted/k] per slot, zero in padding,
  *                    columns interleaved within every group of 8 (below)
