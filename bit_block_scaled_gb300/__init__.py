@@ -6,4 +6,4 @@ from ._lib import (ACT, FMT, LAYOUT, ROUTE, STATUS, Act, MoeError, QWeight, act,
                    moe_grouped_gemm1_act, moe_grouped_gemm2_weighted, moe_last_launch_count,
                    moe_padded_rows, moe_read_status, moe_route_topk, moe_status_string,
                    moe_unpermute_reduce, moe_workspace_size, qweight, moe_import_gptq_int4,
-                   moe_import_modelopt_global_scale)
+                   moe_import_modelopt_global_scale, moe_wait_selftest)

@@ -23,7 +23,7 @@ STATUS_BYTES = 256
 #: symbols include/moe4.h declares
 EXPORTS = ("moe_padded_rows", "moe_workspace_size", "moe_route_topk", "moe_align_permute",
            "moe_grouped_gemm1_act", "moe_grouped_gemm2_weighted", "moe_unpermute_reduce",
-           "moe_forward", "moe_forward_host", "moe_read_status", "moe_clear_status",
+           "moe_forward", "moe_forward_host", "moe_read_status", "moe_clear_status", "moe_wait_selftest",
            "moe_status_string", "moe_last_launch_count", "moe_forward_static", "moe_forward_profile",
            "moe_import_gptq_int4", "moe_import_modelopt_global_scale")
 
@@ -66,6 +66,7 @@ _SIGS = {
                            [_i32, Act, _i32, _i32, _vp, _vp, _vp]),
     "moe_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "moe_clear_status": (_i32, [_vp, _vp]),
+    "moe_wait_selftest": (_i32, [_vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_i32]),
     "moe_last_launch_count": (_i32, []),
     "moe_import_gptq_int4": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
@@ -236,6 +237,10 @@ def moe_read_status(ws, stream=None):
 
 def moe_clear_status(ws, stream=None):
     _check(load().moe_clear_status(_ptr(ws), _stream(stream)), "moe_clear_status")
+
+
+def moe_wait_selftest(ws, stream=None):
+    _check(load().moe_wait_selftest(_ptr(ws), _stream(stream)), "moe_wait_selftest")
 
 
 def moe_status_string(code):

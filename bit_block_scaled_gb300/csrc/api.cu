@@ -65,6 +65,21 @@ T *at(void *ws, size_t off) {
   return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
 }
 
+// A bounded wait that runs out: a barrier initialised for one arrival that
+// never comes. mbar_wait gives up after its cycle limit and the status word
+// records the time-out, as in the layer's kernels.
+__global__ void wait_selftest_kernel(unsigned int *status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(b, 0);
+  if (!ok && threadIdx.x == 0) raise_status(status, MOE_ERR_TIMEOUT);
+}
+
 }  // namespace
 
 extern "C" {
@@ -362,6 +377,14 @@ moe_status_t moe_read_status(const void *ws, moe_stream_t stream, int *status) {
 moe_status_t moe_clear_status(void *ws, moe_stream_t stream) {
   if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
   return cudaMemsetAsync(ws, 0, MOE_STATUS_BYTES, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_wait_selftest(void *ws, moe_stream_t stream) {
+  g_last_launches = 0;
+  if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status_of(ws));
+  ++g_last_launches;
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 const char *moe_status_string(int status) {

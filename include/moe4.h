@@ -293,6 +293,13 @@ moe_status_t moe_read_status(const void *ws, moe_stream_t stream, int *status);
 /* Clears the device status word of `ws` (asynchronous on `stream`). */
 moe_status_t moe_clear_status(void *ws, moe_stream_t stream);
 
+/* Exercises the failure path of the kernels' bounded waits: one single-warp
+ * kernel waits on a shared-memory barrier that nothing arrives on, gives up
+ * after the same cycle limit the layer's waits use (about a second), latches
+ * MOE_ERR_TIMEOUT in the status word of `ws` and returns; the context stays
+ * usable. Asynchronous on `stream`; for tests. */
+moe_status_t moe_wait_selftest(void *ws, moe_stream_t stream);
+
 /* Readable name of a status code (static string). */
 const char *moe_status_string(int status);
 
