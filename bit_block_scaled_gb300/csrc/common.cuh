@@ -110,6 +110,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// The same wait for a role that is off the critical path (the weight
+// producer waiting for a free slot, the epilogue waiting for its next
+// accumulator): between tries it backs off with nanosleep, up to 256 ns, and
+// leaves its issue slots to the dequantisation warps on the same sub-partition.
+__device__ __forceinline__ bool mbar_wait_relaxed(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  unsigned ns = 32;
+  while (true) {
+    __nanosleep(ns);
+    if (ns < 256) ns <<= 1;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
 // Named barrier over `nthreads` threads (whole warps) that also ANDs a
 // predicate across them: every participant gets the same decision. Lets one
 // lead warp poll an mbarrier while the rest of its group blocks in hardware.

@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(cta_threads(KPB), 1) grouped_gemm_kernel(const
       tile_rows(mt, wrow0, wrow1);
       const uint32_t rows1 = wrow1 < p.N ? 64 : 0;
       // block scales of this tile into scale buffer rsc.slot
-      ok = ntiles < 2 || mbar_wait(scempty_bar(rsc.slot), rsc.phase ^ 1);
+      ok = ntiles < 2 || mbar_wait_relaxed(scempty_bar(rsc.slot), rsc.phase ^ 1);
       ok = __all_sync(0xffffffffu, ok && !misc[1]);
       if (!ok) {
         fail(leader);
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(cta_threads(KPB), 1) grouped_gemm_kernel(const
       }
       rsc.advance(2);
       for (int st = 0; st < NS; ++st) {
-        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait(wempty_bar(rst.slot), rst.phase ^ 1);
+        ok = !((issued_mask >> rst.slot) & 1u) || mbar_wait_relaxed(wempty_bar(rst.slot), rst.phase ^ 1);
         ok = __all_sync(0xffffffffu, ok && !misc[1]);
         if (!ok) {
           fail(leader);
@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(cta_threads(KPB), 1) grouped_gemm_kernel(const
       float bias = 0.f;
       if (p.bias && col_ok) bias = bf16_bits_to_float(p.bias[(size_t)e * p.N + n_w]);
       bool lok = true;
-      if (lead) lok = mbar_wait(accfull_bar(rc.slot), rc.phase) && !misc[1];
+      if (lead) lok = mbar_wait_relaxed(accfull_bar(rc.slot), rc.phase) && !misc[1];
       ok = bar_and(kBarEpi, kEpiThreads, lok);
       if (!ok) {
         fail(lead && lane == 0);
