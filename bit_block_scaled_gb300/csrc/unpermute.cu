@@ -44,10 +44,16 @@ __global__ void __launch_bounds__(kUnpermMaxThreads) unpermute_kernel(const uint
   if (!ok && threadIdx.x == 0 && blockIdx.y == 0) raise_status(status, MOE_ERR_BAD_INDEX);
   const int v = blockIdx.y * blockDim.x + threadIdx.x;
   if (v < H8) {
+    // all k rows' loads first (streaming: y is read once), then the sum in
+    // ascending j
+    uint4 q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      q[j] = (j < k && pos[j] >= 0 && pos[j] < P_max) ? __ldcs(&y[(size_t)pos[j] * H8 + v]) : make_uint4(0, 0, 0, 0);
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (j < k && pos[j] >= 0 && pos[j] < P_max) acc8(a, y[(size_t)pos[j] * H8 + v]);
+      if (j < k && pos[j] >= 0 && pos[j] < P_max) acc8(a, q[j]);
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
