@@ -3,11 +3,12 @@
 // weights", "Minimal repro": moe_align_block_size and the sorted_ids /
 // expert_ids it produces).
 //
-// align_kernel is one CTA of 1024 threads. Warp w owns the contiguous flat rows
-// [w * R / 32, (w + 1) * R / 32) and walks them in order, 32 at a time:
+// align_kernel is one CTA of W warps (8 up to 1024 routed rows, else 32). Warp
+// w owns the contiguous flat rows [w * R / W, (w + 1) * R / W) and walks them
+// in order, 32 at a time:
 //   1. per-warp expert counts (__match_any_sync groups equal ids in a step);
 //   2. a warp prefix sum of the block-padded totals gives expert_offsets, and
-//      a per-expert prefix over the 32 warps gives each warp's first slot;
+//      a per-expert prefix over the W warps gives each warp's first slot;
 //   3. each warp walks its rows again and places every row at its expert's
 //      running slot.
 // The order inside an expert is ascending flat row id by construction, so the
@@ -34,7 +35,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__r
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r_lo = (int)((long long)R * warp / 32), r_hi = (int)((long long)R * (warp + 1) / 32);
+  const int nwarps = blockDim.x >> 5, nthr = blockDim.x;
+  const int r_lo = (int)((long long)R * warp / nwarps), r_hi = (int)((long long)R * (warp + 1) / nwarps);
 
   // 1. per-warp counts, in row order
   for (int e = lane; e < E; e += 32) wcnt[warp * E + e] = 0;
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__r
       const int e = e0 + lane;
       int c = 0;
       if (e < E)
-        for (int w = 0; w < 32; ++w) c += wcnt[w * E + e];
+        for (int w = 0; w < nwarps; ++w) c += wcnt[w * E + e];
       const int pc = (c + bm - 1) / bm * bm;
       int incl = pc;
 #pragma unroll
@@ -76,18 +78,18 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t *__r
     if (lane == 0) off[E] = running;
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kAlignThreads) {
+  for (int e = tid; e < E; e += nthr) {
     int run = off[e];
-    for (int w = 0; w < 32; ++w) {
+    for (int w = 0; w < nwarps; ++w) {
       const int c = wcnt[w * E + e];
       wcnt[w * E + e] = run;
       run += c;
     }
   }
-  for (int e = tid; e <= E; e += kAlignThreads) offsets[e] = off[e];
-  for (int q = tid; q < P_max; q += kAlignThreads) sorted[q] = R;
+  for (int e = tid; e <= E; e += nthr) offsets[e] = off[e];
+  for (int q = tid; q < P_max; q += nthr) sorted[q] = R;
   const int nb = P_max / bm;
-  for (int b = tid; b < nb; b += kAlignThreads) {
+  for (int b = tid; b < nb; b += nthr) {
     const int s = b * bm;
     int be = -1;
     if (s < off[E]) {
@@ -382,7 +384,9 @@ moe_status_t launch_align(const int32_t *ids, int T, int k, int E, int block_m, 
     if (launches) ++*launches;
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
-  const cudaError_t err = launch_pdl(align_kernel, dim3(1), dim3(kAlignThreads), 0, stream, ids, R, E, block_m,
+  // up to 1024 rows: 8 warps (a shorter per-expert prefix over the warps)
+  const int threads = R <= 1024 ? 256 : kAlignThreads;
+  const cudaError_t err = launch_pdl(align_kernel, dim3(1), dim3(threads), 0, stream, ids, R, E, block_m,
                                      P_max, sorted_ids, offsets, block_ids, row_pos, status);
   if (launches) ++*launches;
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
