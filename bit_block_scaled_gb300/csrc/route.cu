@@ -22,12 +22,12 @@ namespace moe4 {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kMaxPerLane = 8;  // E <= 256
 constexpr int kMaxK = 8;
 
 __device__ __forceinline__ float sigmoid_f32(float l) { return 1.0f / (1.0f + expf(-l)); }
 
-template <int ROUTE>
+// PL: expert scores per lane, ceil(E / 32) rounded up to 1, 2, 4 or 8 (E <= 256)
+template <int ROUTE, int PL>
 __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restrict__ logits,
                                                             const float *__restrict__ sel_bias, int T, int E,
                                                             int k, int32_t *__restrict__ ids,
@@ -38,9 +38,9 @@ __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restr
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= T) return;
   const float *row = logits + (size_t)t * E;
-  float sc[kMaxPerLane];
+  float sc[PL];
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < PL; ++i) {
     const int e = lane + 32 * i;
     float v = -INFINITY;
     if (e < E) {
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restr
     float best = -INFINITY;
     int bid = 0x7FFFFFFF;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
       if (e < E && !((taken >> i) & 1u) && (sc[i] > best || (sc[i] == best && e < bid))) {
         best = sc[i];
@@ -130,12 +130,19 @@ moe_status_t launch_route(const float *logits, const float *sel_bias, int T, int
   (void)status;
   if (T == 0) return MOE_OK;
   const dim3 grid((T + kWarps - 1) / kWarps), block(kWarps * 32);
-  const cudaError_t err =
-      route == MOE_ROUTE_SIGMOID_BIAS
-          ? launch_pdl(route_kernel<MOE_ROUTE_SIGMOID_BIAS>, grid, block, 0, stream, logits, sel_bias, T, E, k, ids,
-                       weights)
-          : launch_pdl(route_kernel<MOE_ROUTE_TOPK_SOFTMAX>, grid, block, 0, stream, logits, sel_bias, T, E, k, ids,
-                       weights);
+  auto go = [&](auto kern) {
+    return launch_pdl(kern, grid, block, 0, stream, logits, sel_bias, T, E, k, ids, weights);
+  };
+  const bool sig = route == MOE_ROUTE_SIGMOID_BIAS;
+  cudaError_t err;
+  if (E <= 32)
+    err = sig ? go(route_kernel<MOE_ROUTE_SIGMOID_BIAS, 1>) : go(route_kernel<MOE_ROUTE_TOPK_SOFTMAX, 1>);
+  else if (E <= 64)
+    err = sig ? go(route_kernel<MOE_ROUTE_SIGMOID_BIAS, 2>) : go(route_kernel<MOE_ROUTE_TOPK_SOFTMAX, 2>);
+  else if (E <= 128)
+    err = sig ? go(route_kernel<MOE_ROUTE_SIGMOID_BIAS, 4>) : go(route_kernel<MOE_ROUTE_TOPK_SOFTMAX, 4>);
+  else
+    err = sig ? go(route_kernel<MOE_ROUTE_SIGMOID_BIAS, 8>) : go(route_kernel<MOE_ROUTE_TOPK_SOFTMAX, 8>);
   if (launches) ++*launches;
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
